@@ -1,0 +1,253 @@
+"""Pins for the oracle's rejection-sampling tree walk (CPU only).
+
+  * hand-worked cases (tests/golden/verifier_hand.json) computed from the rules of
+    statistical-learning-notes ch.07 "Speculative Decoding", section "Draft Token
+    Validation", and the Sequoia summary, section "Robust Sampling";
+  * losslessness: the emitted tokens follow the target distribution (vLLM PR
+    #2188 "Feature list": rejection sampling guarantees the target model's
+    distribution) -- chi-square over 10^6 seeded trials on a 16-token vocabulary,
+    for a chain, for siblings drafted without replacement, and at T = 0.6, on the
+    first token and on the second token given the first;
+  * p == q accepts every draft (SGLang "SpeculativeDecoding", case "Full Match");
+  * T = 0 reduces to greedy argmax matching, checked against an independent walk;
+  * no match returns exactly one target token, and the page's prefix-match example
+    ("and it's so hot" vs "and it's very warm") keeps the first two drafts.
+Planted mistakes (q kept fixed between siblings, residual left unnormalised,
+residual skipped) must fail the chi-square pin.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+from scipy import stats
+
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "verifier_hand.json")
+
+
+def _softmax64(x, T):
+    z = np.asarray(x, np.float64) / T
+    z = z - z.max(axis=-1, keepdims=True)
+    e = np.exp(z)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
+def _inp(logits, probs, tokens, parent, ua, ub, T):
+    logits = np.ascontiguousarray(logits, np.float32)
+    B, N, V = logits.shape
+    return dict(B=B, N=N, V=V, T=T, target_logits=logits,
+                draft_probs=None if probs is None else np.ascontiguousarray(probs, np.float32),
+                draft_tokens=np.ascontiguousarray(tokens, np.int32),
+                parent=np.ascontiguousarray(parent, np.int32),
+                u_accept=np.ascontiguousarray(ua, np.float32), u_bonus=np.ascontiguousarray(ub, np.float32))
+
+
+# ----------------------------------------------------------------------------- hand-worked
+
+def _golden_cases():
+    g = json.load(open(GOLDEN))
+    for c in g["cases"]:
+        yield g, c
+
+
+@pytest.mark.parametrize("case", [c["name"] for _, c in _golden_cases()])
+def test_hand_worked_cases(oracle_mod, case):
+    g, c = next((g, c) for g, c in _golden_cases() if c["name"] == case)
+    V, parent = g["V"], np.array(g["parent"])
+    N = len(parent)
+    logits = np.log(np.array(g["probs_target"], np.float64))[None]
+    probs = np.array(g["draft_probs"], np.float64)
+    for k, row in c.get("draft_probs_override", {}).items():
+        probs[int(k)] = row
+    r = oracle_mod.tree_reject_sample(_inp(logits, probs[None], [c["tokens"]], parent[None],
+                                           [c["u_accept"]], [c["u_bonus"]], c["T"]))
+    assert r["err"][0] == 0
+    assert list(r["accepted_nodes"][0]) == c["accepted_nodes"]
+    assert r["accept_len"][0] == c["accept_len"]
+    assert r["bonus_token"][0] == c["bonus_token"]
+    assert list(r["out_tokens"][0]) == c["out_tokens"]
+    for j, want in enumerate(c["ratio"]):
+        got = r["ratio"][0, j]
+        if want is None:
+            assert np.isnan(got)
+        elif want == "inf":
+            assert np.isinf(got)
+        else:
+            assert abs(got - want) < 1e-6, (j, got, want)
+    assert V == 3 and N == 4
+
+
+# ----------------------------------------------------------------------------- losslessness
+
+def _markov_trials(rng, n, parent, V, T, tgt_table, drf_table, x0):
+    """n independent verification trials of one tree topology.  The target and
+    draft distributions after a node depend only on that node's token (a Markov
+    target), so the emitted chain must follow softmax(tgt_table[x] / T)."""
+    N = len(parent)
+    kids = [[] for _ in range(N)]
+    for c in range(1, N):
+        kids[parent[c]].append(c)
+    tok = np.empty((n, N), np.int64)
+    tok[:, 0] = x0
+    for i in range(N):
+        if not kids[i]:
+            continue
+        q = drf_table[tok[:, i]].astype(np.float64)
+        with np.errstate(divide="ignore"):
+            key = np.log(q) + rng.gumbel(size=q.shape)
+        top = np.argsort(-key, axis=1, kind="stable")[:, :len(kids[i])]
+        tok[:, kids[i]] = top
+    logits = tgt_table[tok]
+    probs = drf_table[tok]
+    ua = rng.random((n, N), dtype=np.float32)
+    ub = rng.random(n, dtype=np.float32)
+    return _inp(logits, probs, tok, np.tile(parent, (n, 1)), ua, ub, T)
+
+
+def _chi2_pvalues(oracle_mod, parent, T, trials=1_000_000, chunk=200_000, seed=0, mutant=0, V=16):
+    rng = np.random.default_rng(seed)
+    tgt_table = rng.normal(0.0, 1.0, (V, V)).astype(np.float32)
+    drf_logits = tgt_table + rng.normal(0.0, 0.8, (V, V)).astype(np.float32)
+    drf_table = _softmax64(drf_logits, T).astype(np.float32)
+    x0 = 3
+    first = np.zeros(V, np.int64)
+    pair = np.zeros((V, V), np.int64)
+    for s in range(0, trials, chunk):
+        inp = _markov_trials(rng, min(chunk, trials - s), np.array(parent), V, T, tgt_table, drf_table, x0)
+        r = oracle_mod.tree_reject_sample(inp, mutant=mutant)
+        assert not r["err"].any()
+        ot = r["out_tokens"]
+        if (ot[:, 0] < 0).any():  # no token emitted at all: not a distribution over the vocab
+            return 0.0, 0.0, first
+        first += np.bincount(ot[:, 0], minlength=V)
+        two = r["accept_len"] >= 1
+        np.add.at(pair, (ot[two, 0], ot[two, 1]), 1)
+    p_first = _softmax64(tgt_table[x0], T)
+    p1 = stats.chisquare(first, p_first * first.sum()).pvalue
+    stat, dof = 0.0, 0
+    p_next = _softmax64(tgt_table, T)
+    for x in range(V):
+        m = pair[x].sum()
+        if m >= 200:
+            stat += stats.chisquare(pair[x], p_next[x] * m).statistic
+            dof += V - 1
+    p2 = stats.chi2.sf(stat, dof) if dof else 1.0
+    return p1, p2, first
+
+
+CHAIN = [-1, 0, 1, 2]
+SIBLINGS = [-1, 0, 0, 0, 1, 1, 2, 2, 3, 3]  # 3 siblings drafted without replacement, depth 2
+
+
+@pytest.mark.parametrize("parent,T", [(CHAIN, 1.0), (SIBLINGS, 1.0), (SIBLINGS, 0.6)],
+                         ids=["chain_T1", "siblings_T1", "siblings_T0.6"])
+def test_output_follows_target_distribution(oracle_mod, parent, T):
+    p1, p2, first = _chi2_pvalues(oracle_mod, parent, T)
+    assert first.sum() == 1_000_000
+    assert p1 > 1e-3, p1
+    assert p2 > 1e-3, p2
+
+
+@pytest.mark.parametrize("mutant", [1, 2, 5])
+def test_planted_sampler_mistakes_fail_chi_square(oracle_mod, mutant):
+    p1, p2, _ = _chi2_pvalues(oracle_mod, SIBLINGS, 1.0, trials=400_000, mutant=mutant)
+    assert min(p1, p2) < 1e-6, (p1, p2)
+
+
+# ----------------------------------------------------------------------------- special cases
+
+def test_p_equals_q_accepts_every_draft(oracle_mod):
+    rng = np.random.default_rng(1)
+    B, V, T = 64, 500, 0.8
+    for parent in (np.arange(-1, 7), W.binary_tree(15), W.topk_tree((4, 3, 2, 2, 1, 1), 60)):
+        N = len(parent)
+        logits = rng.normal(0, 2, (B, N, V)).astype(np.float32)
+        probs = _softmax64(logits, T).astype(np.float32)
+        tok = rng.integers(0, V, (B, N))
+        ua = (rng.random((B, N)) * 0.999).astype(np.float32)  # keep u away from the ratio 1 +- 1e-7
+        ub = rng.random(B).astype(np.float32)
+        r = oracle_mod.tree_reject_sample(_inp(logits, probs, tok, np.tile(parent, (B, 1)), ua, ub, T))
+        # the first child of every visited node is accepted: follow first children
+        path = [0]
+        while True:
+            kids = [c for c in range(N) if parent[c] == path[-1]]
+            if not kids:
+                break
+            path.append(kids[0])
+        assert (r["accept_len"] == len(path) - 1).all()
+        assert (r["accepted_nodes"][:, :len(path)] == path).all()
+        # bonus: inverse CDF of the leaf's target distribution (numpy searchsorted)
+        leaf_p = _softmax64(logits[:, path[-1]], T)
+        want = np.array([np.searchsorted(np.cumsum(leaf_p[b]), ub[b], side="right") for b in range(B)])
+        assert (r["bonus_token"] == want).all()
+
+
+def _greedy_walk(logits, tok, parent):
+    N = len(parent)
+    node, path = 0, [0]
+    while True:
+        best = int(np.argmax(logits[node]))
+        nxt = next((c for c in range(node + 1, N) if parent[c] == node and tok[c] == best), None)
+        if nxt is None:
+            return path, best
+        path.append(nxt)
+        node = nxt
+
+
+def test_temperature_zero_is_greedy_matching(oracle_mod):
+    rng = np.random.default_rng(2)
+    B, V = 200, 12
+    parent = W.random_tree(np.random.default_rng(5), 20, 6)
+    N = len(parent)
+    logits = rng.integers(-3, 4, (B, N, V)).astype(np.float32)  # many ties: lowest index wins
+    tok = rng.integers(0, V, (B, N))
+    r = oracle_mod.tree_reject_sample(_inp(logits, None, tok, np.tile(parent, (B, 1)),
+                                           np.zeros((B, N)), np.zeros(B), 0.0))
+    accepted_something = 0
+    for b in range(B):
+        path, bonus = _greedy_walk(logits[b], tok[b], parent)
+        assert list(r["accepted_nodes"][b, :len(path)]) == path
+        assert r["accept_len"][b] == len(path) - 1
+        assert r["bonus_token"][b] == bonus
+        accepted_something += len(path) > 1
+    assert accepted_something > 20
+
+
+def test_no_match_and_prefix_match_examples(oracle_mod):
+    # drafts "and it's so hot" (ids 10 11 12 13) vs target "and it's very warm" (10 11 20 21)
+    V = 32
+    parent = np.arange(-1, 4)
+    logits = np.zeros((1, 5, V), np.float32)
+    for node, best in enumerate([10, 11, 20, 21, 22]):
+        logits[0, node, best] = 5.0
+    tok = np.array([[1, 10, 11, 12, 13]])
+    r = oracle_mod.tree_reject_sample(_inp(logits, None, tok, parent[None], np.zeros((1, 5)), [0.0], 0.0))
+    assert r["accept_len"][0] == 2
+    assert list(r["out_tokens"][0]) == [10, 11, 20, -1, -1]
+    # no match: exactly one token, from the target
+    tok2 = np.array([[1, 9, 11, 12, 13]])
+    r = oracle_mod.tree_reject_sample(_inp(logits, None, tok2, parent[None], np.zeros((1, 5)), [0.0], 0.0))
+    assert r["accept_len"][0] == 0 and list(r["out_tokens"][0]) == [10, -1, -1, -1, -1]
+    # full match: every draft plus one more
+    tok3 = np.array([[1, 10, 11, 20, 21]])
+    r = oracle_mod.tree_reject_sample(_inp(logits, None, tok3, parent[None], np.zeros((1, 5)), [0.0], 0.0))
+    assert r["accept_len"][0] == 4 and list(r["out_tokens"][0]) == [10, 11, 20, 21, 22]
+
+
+def test_error_bits(oracle_mod):
+    rng = np.random.default_rng(4)
+    B, N, V = 5, 7, 50
+    parent = np.tile(W.binary_tree(N), (B, 1))
+    logits = rng.normal(0, 1, (B, N, V)).astype(np.float32)
+    probs = _softmax64(logits + 0.3, 1.0).astype(np.float32)
+    tok = rng.integers(0, V, (B, N))
+    parent[0, 4] = 4        # bad tree
+    tok[1, 1] = V           # token out of range (child 1 of the root is always tried)
+    logits[2, 0, 17] = np.nan  # the root row is always visited
+    probs[3, 0, 3] = np.inf    # the root's draft row is read when its first child is tried
+    r = oracle_mod.tree_reject_sample(_inp(logits, probs, tok, parent, rng.random((B, N)), rng.random(B), 1.0))
+    assert list(r["err"]) == [1, 8, 16, 16, 0]
+    assert list(r["accept_len"][:4]) == [-1] * 4 and r["accept_len"][4] >= 0
+    assert (r["out_tokens"][:4] == -1).all() and (r["bonus_token"][:4] == -1).all()
