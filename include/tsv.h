@@ -1,0 +1,158 @@
+/*
+ * tsv.h -- C ABI of libtsv, the GB300 (sm_103a) target-side verification step of
+ * tree-based speculative decoding.
+ *
+ * One verification step is three calls on one CUDA stream, with no host
+ * synchronisation between them:
+ *   1. tsv_tree_verify_attn    -- attention of the flattened draft tree over the
+ *                                 paged KV cache under the ancestor-only tree mask;
+ *   2. tsv_tree_reject_sample  -- rejection-sampling walk of the tree (Sequoia-style
+ *                                 sampling without replacement) plus a bonus token;
+ *   3. tsv_kv_compact_accepted -- KV-cache rewrite of the accepted path.
+ * (Step 2 consumes target logits, which in a full model are produced from step
+ * 1's output by the layers above attention; the library takes them as input.)
+ *
+ * Conventions for every entry point
+ *  - All array pointers are caller-owned DEVICE memory on the current device,
+ *    except where a comment says otherwise.  The library allocates no device
+ *    memory and keeps no state between calls; calls are thread-safe.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default).
+ *  - Host-side argument errors return TSV_ERR_ARG / TSV_ERR_UNSUPPORTED at once and
+ *    launch nothing.  A failed launch returns TSV_ERR_CUDA.  tsv_last_error()
+ *    gives a message for the calling thread's last failure.
+ *  - Data errors found on the device never trap: they are written as bit masks to
+ *    `seq_err[b]` (one int32 per sequence, overwritten by each call) and the
+ *    sequence's outputs are poisoned as documented per call.
+ *  - Layouts are row-major:  q/out [B, N, Hq, D];  caches [num_blocks, block_size,
+ *    Hkv, D];  block_table [B, max_blocks];  seq_lens/ new_seq_lens [B];  parent,
+ *    draft_tokens, u_accept, accepted_nodes, out_tokens [B, N];  target_logits,
+ *    draft_probs [B, N, V];  u_bonus, accept_len, bonus_token, seq_err [B].
+ *  - Logical slot t of sequence b lives at physical row
+ *    block_table[b, t / block_size] * block_size + t % block_size of the caches.
+ *
+ * The tree (sglang report "Speculative decoding on sglang", sections "What is
+ * Tree-Attention?" and "Tree-based Speculative Decoding (EAGLE) Implementation
+ * Summary": draft candidates flattened to 1-D, verified in one pass under a tree
+ * mask) is given per sequence as parent[b, i]: node 0 is the root, i.e. the last
+ * accepted token (parent -1), and 0 <= parent[i] < i for i >= 1.  Node i's K/V is
+ * already in the cache at logical slot seq_lens[b] + i (written by the caller's
+ * projection, as serving engines do); the caller preallocates the blocks, so
+ * seq_lens[b] + N <= max_blocks * block_size ("preallocated slots", vLLM PR #2188,
+ * "Guide for reviewers").
+ */
+#ifndef TSV_H
+#define TSV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TSV_OK = 0,
+    TSV_ERR_ARG = 1,         /* null pointer, bad size, workspace too small */
+    TSV_ERR_UNSUPPORTED = 2, /* valid but not built: e.g. D not in {64, 128} */
+    TSV_ERR_CUDA = 3         /* a CUDA runtime/driver call or launch failed */
+} tsv_status;
+
+typedef enum { TSV_BF16 = 0, TSV_F32 = 1 } tsv_dtype;
+
+/* Device-side data error bits written to seq_err[b]. */
+enum {
+    TSV_DERR_PARENT = 1,    /* parent array (or accepted path) is not a valid tree/path */
+    TSV_DERR_BLOCK = 2,     /* a block id covering slots [0, L_b + N) is outside [0, num_blocks) */
+    TSV_DERR_CAPACITY = 4,  /* L_b < 0 or L_b + N > max_blocks * block_size */
+    TSV_DERR_TOKEN = 8,     /* a tried draft token is outside [0, V) */
+    TSV_DERR_NONFINITE = 16 /* a visited logits row, or a draft row that is read, is not finite */
+};
+
+/* Message for the calling thread's most recent failed call ("" if none). */
+const char *tsv_last_error(void);
+
+/* ---------------------------------------------------------------------------
+ * Tree-masked GQA attention (sglang report, "What is Tree-Attention?"; the EAGLE
+ * "Tree Decoding" step with attention_mask + tree_attention_mask).
+ *
+ * For query row (b, n, h), kv head g = h / (Hq / Hkv):
+ *   keys = prefix slots 0 .. L_b-1  (all visible)
+ *        + tree slots L_b + j for every node j on the root-to-n path, n included;
+ *   out[b,n,h,:] = softmax_t(scale * q[b,n,h,:] . k[t,g,:]) @ v[t,g,:].
+ * q, caches and out share `dtype` (bf16: tensor-core tiles, fp32 accumulation;
+ * fp32: exact fp32 FMA path).  D in {64, 128}; 1 <= N <= 128; Hq % Hkv == 0;
+ * block_size a power of two in [8, 128].
+ * Long prefixes are split into key chunks whose partial (max, sum, output) go to
+ * `workspace` and are merged by a second kernel; `workspace` must hold
+ * tsv_attn_workspace_size(...) bytes (may be NULL when that is 0) and is
+ * scratch owned by the caller, not read before it is written.
+ * Rows of a sequence with seq_err != 0 are written as NaN.
+ * Cache slots from L_b + N to the end of the sequence's last block are never
+ * read into the result (they may hold anything, NaN included).
+ * ------------------------------------------------------------------------- */
+size_t tsv_attn_workspace_size(int B, int N, int Hq, int Hkv, int D, int block_size, int max_blocks,
+                               tsv_dtype dtype);
+
+tsv_status tsv_tree_verify_attn(const void *q, const void *k_cache, const void *v_cache,
+                                const int32_t *block_table, const int32_t *seq_lens,
+                                const int32_t *parent, void *out, int B, int N, int Hq, int Hkv,
+                                int D, int block_size, int max_blocks, int num_blocks, float scale,
+                                tsv_dtype dtype, void *workspace, size_t workspace_bytes,
+                                int32_t *seq_err, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Rejection-sampling verification of the tree (statistical-learning-notes ch.07
+ * "Speculative Decoding", section "Draft Token Validation"; Sequoia summary,
+ * sections "Scalable Speculative Decoding" and "Robust Sampling").
+ *
+ * Per sequence, starting at the root i = 0:
+ *   p = softmax(target_logits[b,i,:] / T), q = draft_probs[b,i,:];
+ *   children c of i are tried in increasing index with x = draft_tokens[b,c]:
+ *     accept iff u_accept[b,c] < p(x)/q(x)   (q(x) == 0: accept iff p(x) > 0);
+ *     on rejection p <- normalize(max(0, p - q)) (kept if that sum is 0),
+ *                  q(x) <- 0, q <- normalize(q) (kept if that sum is 0);
+ *   the first accepted child becomes i; when no child is accepted (or i is a
+ *   leaf) the walk stops and the bonus token is the smallest t with
+ *   u_bonus[b] < sum_{v<=t} p(v) over the current p (last t with p(t) > 0 if none).
+ * T == 0: a child is accepted iff its token is argmax target_logits[b,i,:]
+ * (lowest index on ties) and the bonus is that argmax; draft_probs and the
+ * uniforms are not read (draft_probs may be NULL).
+ * Outputs: accepted_nodes[b,:] = root-first path, -1 padded; accept_len[b] =
+ * drafts accepted (path length - 1); bonus_token[b]; out_tokens[b,:] = accepted
+ * draft tokens then the bonus, -1 padded.  A sequence with seq_err != 0 gets
+ * accept_len = bonus_token = -1 and all-(-1) rows.
+ * Uniforms are pre-drawn by the caller in [0, 1).  Vocabulary-wide sums use fp32
+ * per thread and fp64 across threads; the ratio p(x)/q(x) itself is evaluated in
+ * fp64.  V <= 16 * 1024 * 32.
+ * ------------------------------------------------------------------------- */
+tsv_status tsv_tree_reject_sample(const float *target_logits, const float *draft_probs,
+                                  const int32_t *draft_tokens, const int32_t *parent,
+                                  const float *u_accept, const float *u_bonus, float temperature,
+                                  int B, int N, int V, int32_t *accepted_nodes, int32_t *accept_len,
+                                  int32_t *bonus_token, int32_t *out_tokens, int32_t *seq_err,
+                                  void *stream);
+
+/* ---------------------------------------------------------------------------
+ * KV-cache rewrite for the accepted path (sglang report: the KV cache must be
+ * updated selectively for accepted indices and trees require a rewrite; SGLang
+ * "SpeculativeDecoding", prefix match: rejected tokens' KV cache is evicted).
+ *
+ * For j = 1 .. accept_len[b]: the K and V rows (all kv heads) at logical slot
+ * L_b + accepted_nodes[b,j] move to logical slot L_b + j; new_seq_lens[b] =
+ * L_b + 1 + accept_len[b].  Slots at or past the new length are evicted by the
+ * length cut (their bytes are not cleared; freeing blocks is the caller's).
+ * seq_lens is read only, so a repeated call gives the same result.
+ * accept_len[b] < 0 leaves the sequence untouched (new_seq_lens[b] = L_b).
+ * The path must satisfy 0 = a_0 < a_1 < ... < a_A < N (else TSV_DERR_PARENT).
+ * ------------------------------------------------------------------------- */
+tsv_status tsv_kv_compact_accepted(void *k_cache, void *v_cache, const int32_t *block_table,
+                                   const int32_t *seq_lens, const int32_t *accepted_nodes,
+                                   const int32_t *accept_len, int32_t *new_seq_lens, int B, int N,
+                                   int Hkv, int D, int block_size, int max_blocks, int num_blocks,
+                                   tsv_dtype dtype, int32_t *seq_err, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TSV_H */

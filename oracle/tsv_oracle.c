@@ -45,7 +45,9 @@
  *
  * Error bits (per sequence, OR-ed): 1 bad tree/path, 2 block id out of range,
  * 4 capacity (L_b + N > max_blocks * block_size, or L_b < 0), 8 token out of range,
- * 16 non-finite logits/probabilities.  A failed sequence gets accept_len = -1.
+ * 16 non-finite logits/probabilities (a visited logits row; the drafted token's
+ * draft probability; a node's whole draft row once a residual is formed there).
+ * A failed sequence gets accept_len = -1.
  */
 #include <math.h>
 #include <stdint.h>
@@ -315,19 +317,21 @@ int oracle_tree_reject_sample(const float *target_logits, const float *draft_pro
                     }
                     continue;
                 }
-                if (!q_loaded) {
-                    /* the draft distribution of node i's children, promoted to double */
-                    if (!row_is_finite(qrow, V)) {
+                /* q(x): node i's draft probability of the drafted token; the whole
+                 * row is read only once a residual has to be formed */
+                double qx;
+                if (q_loaded) {
+                    qx = qv[x];
+                } else {
+                    if (!isfinite(qrow[x])) {
                         err = ERR_NONFINITE;
                         break;
                     }
-                    for (int v = 0; v < V; v++)
-                        qv[v] = (double)qrow[v];
-                    q_loaded = 1;
+                    qx = (double)qrow[x];
                 }
                 double r;
-                if (qv[x] > 0.0)
-                    r = p[x] / qv[x];
+                if (qx > 0.0)
+                    r = p[x] / qx;
                 else
                     r = (p[x] > 0.0) ? INFINITY : 0.0;
                 if (ratio)
@@ -335,6 +339,15 @@ int oracle_tree_reject_sample(const float *target_logits, const float *draft_pro
                 if ((double)u_accept[(int64_t)b * N + c] < r) {
                     next = c;
                     break;
+                }
+                if (!q_loaded) {
+                    if (!row_is_finite(qrow, V)) {
+                        err = ERR_NONFINITE;
+                        break;
+                    }
+                    for (int v = 0; v < V; v++)
+                        qv[v] = (double)qrow[v];
+                    q_loaded = 1;
                 }
                 /* rejected: residual p <- normalize(max(0, p - q)) */
                 double zr = 0.0;

@@ -243,11 +243,24 @@ def test_error_bits(oracle_mod):
     logits = rng.normal(0, 1, (B, N, V)).astype(np.float32)
     probs = _softmax64(logits + 0.3, 1.0).astype(np.float32)
     tok = rng.integers(0, V, (B, N))
+    B = 7
+    parent = np.tile(W.binary_tree(N), (B, 1))
+    logits = rng.normal(0, 1, (B, N, V)).astype(np.float32)
+    probs = _softmax64(logits + 0.3, 1.0).astype(np.float32)
+    tok = rng.integers(0, V, (B, N))
+    ua = rng.random((B, N))
     parent[0, 4] = 4        # bad tree
     tok[1, 1] = V           # token out of range (child 1 of the root is always tried)
     logits[2, 0, 17] = np.nan  # the root row is always visited
-    probs[3, 0, 3] = np.inf    # the root's draft row is read when its first child is tried
-    r = oracle_mod.tree_reject_sample(_inp(logits, probs, tok, parent, rng.random((B, N)), rng.random(B), 1.0))
-    assert list(r["err"]) == [1, 8, 16, 16, 0]
-    assert list(r["accept_len"][:4]) == [-1] * 4 and r["accept_len"][4] >= 0
-    assert (r["out_tokens"][:4] == -1).all() and (r["bonus_token"][:4] == -1).all()
+    probs[3, 0, tok[3, 1]] = np.inf  # the drafted token's q is read when child 1 is tried
+    # a non-finite draft row matters only once a residual is formed: sequence 4 rejects
+    # child 1 at the root (p(x) ~ 0), sequence 5 accepts it (p(x) ~ 1)
+    logits[4, 0, tok[4, 1]] = -30.0
+    probs[4, 0, (tok[4, 1] + 1) % V] = np.nan
+    logits[5, 0, tok[5, 1]] = 30.0
+    ua[5, 1] = 0.5
+    probs[5, 0, (tok[5, 1] + 1) % V] = np.nan
+    r = oracle_mod.tree_reject_sample(_inp(logits, probs, tok, parent, ua, rng.random(B), 1.0))
+    assert list(r["err"]) == [1, 8, 16, 16, 16, 0, 0]
+    assert list(r["accept_len"][:5]) == [-1] * 5 and (r["accept_len"][5:] >= 0).all()
+    assert (r["out_tokens"][:5] == -1).all() and (r["bonus_token"][:5] == -1).all()

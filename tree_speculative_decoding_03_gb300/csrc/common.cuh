@@ -1,0 +1,72 @@
+// common.cuh -- small device helpers shared by the libtsv kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/tsv.h"
+
+namespace tsv {
+
+constexpr int kMaxNodes = 128;  // tree nodes per sequence, root included
+
+// Validates one sequence's tree: parent[0] == -1 and 0 <= parent[i] < i.
+// Cooperative over the calling block; every thread gets the same answer.
+__device__ __forceinline__ bool block_tree_ok(const int32_t* par, int N, int* s_flag) {
+    if (threadIdx.x == 0) *s_flag = 1;
+    __syncthreads();
+    for (int i = threadIdx.x; i < N; i += blockDim.x) {
+        int p = par[i];
+        bool ok = (i == 0) ? (p == -1) : (p >= 0 && p < i);
+        if (!ok) *s_flag = 0;
+    }
+    __syncthreads();
+    bool r = *s_flag != 0;
+    __syncthreads();
+    return r;
+}
+
+// Capacity and block-id checks for logical slots [0, L + N) of one sequence;
+// returns TSV_DERR_CAPACITY, TSV_DERR_BLOCK or 0 (capacity is checked first).
+__device__ __forceinline__ int block_cache_errors(const int32_t* bt_row, int L, int N, int bs,
+                                                  int max_blocks, int num_blocks, int* s_flag) {
+    if ((long long)L < 0 || (long long)L + N > (long long)max_blocks * bs) return TSV_DERR_CAPACITY;
+    if (threadIdx.x == 0) *s_flag = 0;
+    __syncthreads();
+    int nblk = (L + N + bs - 1) / bs;
+    for (int j = threadIdx.x; j < nblk; j += blockDim.x) {
+        int id = bt_row[j];
+        if (id < 0 || id >= num_blocks) *s_flag = TSV_DERR_BLOCK;
+    }
+    __syncthreads();
+    int r = *s_flag;
+    __syncthreads();
+    return r;
+}
+
+// Ancestor masks of the tree: anc[n] (4 x 32 bits) has bit j set iff node j is on the
+// root-to-n path, n included.  Threads n < N each walk up their own path; the walk is
+// bounded by N steps, so an invalid parent array cannot make it loop.
+__device__ __forceinline__ void build_ancestor_masks(const int32_t* par, int N, uint32_t (*anc)[4]) {
+    for (int n = threadIdx.x; n < N; n += blockDim.x) {
+        uint32_t m[4] = {0u, 0u, 0u, 0u};
+        int a = n;
+        for (int step = 0; step <= N && a >= 0 && a < N; ++step) {
+            m[a >> 5] |= 1u << (a & 31);
+            a = par[a];
+        }
+        anc[n][0] = m[0];
+        anc[n][1] = m[1];
+        anc[n][2] = m[2];
+        anc[n][3] = m[3];
+    }
+}
+
+__device__ __forceinline__ bool anc_has(const uint32_t* m, int j) { return (m[j >> 5] >> (j & 31)) & 1u; }
+
+// Physical row of logical slot t (block ids already validated by the caller).
+__device__ __forceinline__ long long phys_row(const int32_t* bt_row, int t, int bs_log2) {
+    return (long long)bt_row[t >> bs_log2] * (1 << bs_log2) + (t & ((1 << bs_log2) - 1));
+}
+
+}  // namespace tsv
