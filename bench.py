@@ -1,0 +1,435 @@
+#!/usr/bin/env python
+"""Benchmark of one tree-verification step on GB300.
+
+A step is one pass of the whole hot path over one synthetic batch, on one CUDA
+stream: tsv_tree_verify_attn (tree-masked attention + split-K merge),
+tsv_tree_reject_sample (rejection-sampling walk + bonus token) and
+tsv_kv_compact_accepted (KV rewrite of the accepted path).
+
+Metric: verified draft-tree tokens per second = B * N tree tokens (root included)
+per step / device time per step.  The workload defaults to the chain
+configuration (batch 8, 32/8 heads, D 128, bf16 paged KV, prefix 2048, K = 5
+drafts, vocabulary 128256, T = 1).  L2 is flushed (256 MB write) between timed
+steps; each step is timed with CUDA events on its stream and the step times are
+summed.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config I] [--impl ours|reference]
+
+Under torchrun each rank runs its own independent batch on its own GPU (replicas,
+no collective on the data path); rank 0 prints one JSON line.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import glob
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "verified draft-tree tokens/sec per verify step"
+UNIT = "tokens/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _source_digest():
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "tree_speculative_decoding_03_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic_record(kernel, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            recs = json.load(f)
+    except Exception:
+        return None
+    for r in recs:
+        if r.get("kernel") == kernel and r.get("workload") == workload and r.get("source_digest") == _source_digest():
+            return r.get("dram_bytes_per_launch")
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "20"], stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.05)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.out.close()
+
+    def summary(self, t_start, t_end):
+        if self.proc is None or not self.path:
+            return None
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            for name, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(rows), "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- algorithmic work
+
+def attn_bytes(inp):
+    """K/V of every visible slot (prefix + tree) once, plus Q in and O out."""
+    esz = 2 if inp["dtype"] == "bf16" else 4
+    kv = sum(int(L) + inp["N"] for L in inp["seq_lens"]) * inp["Hkv"] * inp["D"] * esz * 2
+    qo = 2 * inp["B"] * inp["N"] * inp["Hq"] * inp["D"] * esz
+    return kv + qo
+
+
+def verify_bytes(inp, accepted_nodes, accept_len):
+    """Rows the walk must read: each visited node's logits row, plus its draft row
+    when a residual is formed there (a child other than the first is accepted, or
+    none is while children exist).  T == 0 reads no draft rows."""
+    V, N = inp["V"], inp["N"]
+    total = 0
+    for b in range(inp["B"]):
+        A = int(accept_len[b])
+        if A < 0:
+            continue
+        path = [int(x) for x in accepted_nodes[b, :A + 1]]
+        par = inp["parent"][b]
+        for j, node in enumerate(path):
+            total += V * 4
+            kids = [c for c in range(node + 1, N) if par[c] == node]
+            if inp["T"] > 0 and kids:
+                nxt = path[j + 1] if j + 1 < len(path) else None
+                if nxt != kids[0]:
+                    total += V * 4
+    return total
+
+
+def compact_bytes(inp, accept_len):
+    esz = 2 if inp["dtype"] == "bf16" else 4
+    rows = sum(max(0, int(a)) for a in accept_len)
+    return rows * inp["Hkv"] * inp["D"] * esz * 2 * 2  # K and V, read + write
+
+
+# ----------------------------------------------------------------------------- oracle leg
+
+def _subset(inp, seqs):
+    s = dict(inp)
+    seqs = np.asarray(seqs)
+    for k in ("parent", "seq_lens", "block_table", "q", "target_logits", "draft_probs", "draft_tokens",
+              "u_accept", "u_bonus"):
+        s[k] = np.ascontiguousarray(inp[k][seqs])
+    s["B"] = len(seqs)
+    return s
+
+
+def oracle_step(inp, seqs):
+    """The whole step on the CPU oracle for the given sequences (single thread)."""
+    import oracle
+    sub = _subset(inp, seqs)
+    oracle.tree_verify_attn(sub)
+    r = oracle.tree_reject_sample(sub)
+    oracle.kv_compact_accepted(sub, r["accepted_nodes"], r["accept_len"], inplace=True)
+
+
+def oracle_sample_plan(inp, budget_s):
+    """Times one sequence, then picks how many sequences fit the time budget."""
+    import oracle
+    oracle.build()
+    scratch = dict(inp)
+    scratch["k_cache"] = np.array(inp["k_cache"], copy=True)
+    scratch["v_cache"] = np.array(inp["v_cache"], copy=True)
+    t0 = time.perf_counter()
+    oracle_step(scratch, [0])
+    t1 = time.perf_counter() - t0
+    n = int(max(1, min(inp["B"], budget_s // max(t1, 1e-6))))
+    return scratch, list(range(n)), t1
+
+
+def cpu_baseline(inp, budget_s=15.0):
+    scratch, seqs, _ = oracle_sample_plan(inp, budget_s)
+    t0 = time.perf_counter()
+    oracle_step(scratch, seqs)
+    dt = time.perf_counter() - t0
+    tokens = len(seqs) * inp["N"]
+    return {"value": tokens / dt, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"full step (attention of all rows, walk, compaction) for {len(seqs)} of {inp['B']} "
+                      f"sequences = {tokens} tree tokens, single-threaded C oracle, fp64"}
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import tree_speculative_decoding_03_gb300 as tsv
+
+    torch.cuda.set_device(local_rank)
+    tsv.build()
+    tsv.load()
+    w = W.CONFIGS[args.config]
+    T = w.T if args.temperature is None else args.temperature
+    inp = W.generate(w, temperature=T, seed=w.seed + 7919 * rank)
+    B, N, Hq, Hkv, D, V = inp["B"], inp["N"], inp["Hq"], inp["Hkv"], inp["D"], inp["V"]
+    bf = inp["dtype"] == "bf16"
+    el = torch.bfloat16 if bf else torch.float32
+
+    def host(x, dtype=None):
+        t = torch.from_numpy(np.ascontiguousarray(x.view(np.int16) if x.dtype == np.uint16 else x))
+        if dtype is not None:
+            t = t.view(dtype)
+        return t.pin_memory()
+
+    H = dict(q=host(inp["q"], el), k_cache=host(inp["k_cache"], el), v_cache=host(inp["v_cache"], el),
+             block_table=host(inp["block_table"]), seq_lens=host(inp["seq_lens"]), parent=host(inp["parent"]),
+             target_logits=host(inp["target_logits"]), draft_probs=host(inp["draft_probs"]),
+             draft_tokens=host(inp["draft_tokens"]), u_accept=host(inp["u_accept"]), u_bonus=host(inp["u_bonus"]))
+    Dv = {k: v.cuda() for k, v in H.items()}
+    out = torch.empty_like(Dv["q"])
+    dt_code = tsv.TSV_BF16 if bf else tsv.TSV_F32
+    ws_bytes = tsv.attn_workspace_size(B, N, Hq, Hkv, D, inp["block_size"], inp["max_blocks"], dt_code)
+    ws = torch.empty(max(16, ws_bytes), dtype=torch.uint8, device="cuda")
+    i32 = dict(dtype=torch.int32, device="cuda")
+    attn_err, samp_err, comp_err = (torch.empty(B, **i32) for _ in range(3))
+    acc_nodes, out_tokens = torch.empty(B, N, **i32), torch.empty(B, N, **i32)
+    acc_len, bonus, new_lens = torch.empty(B, **i32), torch.empty(B, **i32), torch.empty(B, **i32)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        tsv.tree_verify_attn(Dv["q"], Dv["k_cache"], Dv["v_cache"], Dv["block_table"], Dv["seq_lens"],
+                             Dv["parent"], out, inp["scale"], workspace=ws if ws_bytes else None, seq_err=attn_err)
+        if ev is not None:
+            ev[1].record(stream)
+        tsv.tree_reject_sample(Dv["target_logits"], Dv["draft_probs"], Dv["draft_tokens"], Dv["parent"],
+                               Dv["u_accept"], Dv["u_bonus"], T, acc_nodes, acc_len, bonus, out_tokens, samp_err)
+        if ev is not None:
+            ev[2].record(stream)
+        tsv.kv_compact_accepted(Dv["k_cache"], Dv["v_cache"], Dv["block_table"], Dv["seq_lens"], acc_nodes,
+                                acc_len, new_lens, comp_err)
+        if ev is not None:
+            ev[3].record(stream)
+
+    flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")  # 256 MB > 129 MB L2
+    for i in range(args.warmup):
+        flush.fill_(float(i))
+        step()
+    torch.cuda.synchronize()
+    assert not attn_err.any() and not samp_err.any() and not comp_err.any(), "device-side data error"
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        t_wall = time.perf_counter()
+        for k in range(K):
+            flush.fill_(float(k))
+            step(evs[k])
+        barrier()
+        t_wall = time.perf_counter() - t_wall
+    clocks = clk.summary(0, 0)
+    per = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in evs])  # ms
+    step_ms = per.sum(axis=1)
+    dev_s = float(step_ms.sum()) / 1e3
+    if world > 1:
+        t = torch.tensor([dev_s], device="cuda", dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        dev_s = float(t.item())
+    tokens_per_step = B * N
+    value = world * tokens_per_step * K / dev_s
+
+    # decisions of the last step, for the verifier's realised bytes
+    an, al = acc_nodes.cpu().numpy(), acc_len.cpu().numpy()
+    mean_ms = per.mean(axis=0)
+    kernels = {
+        "tree_verify_attn": (attn_bytes(inp), mean_ms[0]),
+        "tree_reject_sample": (verify_bytes(inp, an, al), mean_ms[1]),
+        "kv_compact_accepted": (compact_bytes(inp, al), mean_ms[2]),
+    }
+    dom = max(kernels, key=lambda k: kernels[k][1])
+    peak, peak_kind = _peaks()
+    dom_bytes, dom_ms = kernels[dom]
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": _traffic_record(dom, w.name),
+                "kernel": dom, "peak_source": f"{peak_kind} hbm_gbs",
+                "algorithmic_bytes_per_launch": int(dom_bytes), "avg_launch_us": round(dom_ms * 1e3, 2)}
+    per_kernel = {k: {"avg_us": round(ms * 1e3, 2), "algorithmic_bytes": int(b),
+                      "hbm_frac": round(b / (ms * 1e-3) / 1e9 / peak, 4)} for k, (b, ms) in kernels.items()}
+
+    # end to end through the public API: pinned host inputs in, results out, every step
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    res_host = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (out_tokens, acc_len, bonus, new_lens)]
+    h2d = sum(t.numel() * t.element_size() for t in H.values())
+    d2h = out.numel() * out.element_size() + sum(t.numel() * t.element_size() for t in res_host)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    e0.record(stream)
+    for k in range(K):
+        for name, t in H.items():
+            Dv[name].copy_(t, non_blocking=True)
+        step()
+        out_host.copy_(out, non_blocking=True)
+        for hst, dvc in zip(res_host, (out_tokens, acc_len, bonus, new_lens)):
+            hst.copy_(dvc, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    e2e_s = e0.elapsed_time(e1) / 1e3
+    if world > 1:
+        t = torch.tensor([e2e_s], device="cuda", dtype=torch.float64)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    e2e = {"value": world * tokens_per_step * K / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+           "d2h_bytes_per_step": int(d2h)}
+
+    launches_per_step = 3 + (1 if ws_bytes else 0)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": float(step_ms.mean()), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": inp["dtype"], "data": "synthetic (seeded; stands in for the pages' model/dataset runs)",
+        "config": {"workload": w.name, "B": B, "N": N, "Hq": Hq, "Hkv": Hkv, "D": D, "V": V, "T": T,
+                   "prefix": list(w.prefix), "block_size": inp["block_size"], "tree": w.tree,
+                   "l2": "flushed between timed steps (256 MB write); per-step CUDA events summed",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline,
+        "per_kernel": per_kernel,
+        "e2e": e2e,
+        "gpu_launches": int(launches_per_step * K),
+        "clocks": clocks,
+        "mean_accept_len": float(np.mean(al)),
+        "wall_s_timed_region": t_wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(inp)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- reference arm (the oracle)
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    w = W.CONFIGS[args.config]
+    T = w.T if args.temperature is None else args.temperature
+    inp = W.generate(w, temperature=T)
+    scratch, seqs, t1 = oracle_sample_plan(inp, budget_s=120.0 / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        oracle_step(scratch, seqs)
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle_step(scratch, seqs)
+        times.append(time.perf_counter() - t0)
+    tokens = len(seqs) * inp["N"]
+    value = tokens * len(times) / sum(times)
+    sample = (f"each step: full step (attention of all rows, walk, compaction) for {len(seqs)} of {inp['B']} "
+              f"sequences = {tokens} tree tokens, single-threaded C oracle, fp64")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded)",
+            "config": {"workload": w.name, "B": inp["B"], "N": inp["N"], "T": T, "sampled_sequences": len(seqs)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=1, help="workload index (0..4)")
+    ap.add_argument("--temperature", type=float, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

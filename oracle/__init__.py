@@ -116,13 +116,18 @@ def tree_reject_sample(inp: dict, *, temperature: Optional[float] = None, mutant
 
 
 def kv_compact_accepted(inp: dict, accepted_nodes: np.ndarray, accept_len: np.ndarray, *,
-                        mutant: int = 0):
-    """Array-copy compaction on copies of the caches.  Returns
-    (k_cache, v_cache, new_seq_lens, err)."""
+                        mutant: int = 0, inplace: bool = False):
+    """Array-copy compaction, on copies of the caches unless `inplace` (then the
+    given C-contiguous arrays are modified).  Returns (k_cache, v_cache,
+    new_seq_lens, err)."""
     B, N = inp["B"], inp["N"]
     el = np.float32 if inp["dtype"] == "f32" else np.uint16
-    k = np.array(inp["k_cache"], dtype=el, copy=True, order="C")
-    v = np.array(inp["v_cache"], dtype=el, copy=True, order="C")
+    if inplace:
+        k, v = inp["k_cache"], inp["v_cache"]
+        assert k.dtype == el and v.dtype == el and k.flags.c_contiguous and v.flags.c_contiguous
+    else:
+        k = np.array(inp["k_cache"], dtype=el, copy=True, order="C")
+        v = np.array(inp["v_cache"], dtype=el, copy=True, order="C")
     bt = _c(inp["block_table"], np.int32)
     sl = _c(inp["seq_lens"], np.int32)
     an = _c(accepted_nodes, np.int32)

@@ -1,0 +1,46 @@
+"""The C ABI library builds for sm_103a, loads, and exports every entry point that
+include/tsv.h declares; host-side argument checks answer without a GPU."""
+import ctypes
+
+import pytest
+
+import tree_speculative_decoding_03_gb300 as tsv
+
+
+@pytest.fixture(scope="module")
+def lib():
+    tsv.build()
+    return tsv.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = tsv.header_symbols()
+    assert {"tsv_tree_verify_attn", "tsv_tree_reject_sample", "tsv_kv_compact_accepted",
+            "tsv_attn_workspace_size", "tsv_last_error"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_host_argument_checks_need_no_gpu(lib):
+    P = None
+    # tree too large: rejected before any CUDA call
+    st = lib.tsv_tree_reject_sample(P, P, P, P, P, P, 1.0, 4, 200, 100, P, P, P, P, P, P)
+    assert st == tsv.TSV_ERR_UNSUPPORTED
+    assert b"tree nodes" in lib.tsv_last_error()
+    st = lib.tsv_tree_reject_sample(P, P, P, P, P, P, -1.0, 4, 8, 100, P, P, P, P, P, P)
+    assert st == tsv.TSV_ERR_ARG
+    st = lib.tsv_tree_reject_sample(P, P, P, P, P, P, 1.0, 4, 8, 100, P, P, P, P, P, P)
+    assert st == tsv.TSV_ERR_ARG and b"null" in lib.tsv_last_error()
+    # head dim 96 is not built
+    st = lib.tsv_tree_verify_attn(P, P, P, P, P, P, P, 2, 8, 8, 2, 96, 16, 4, 8, 0.1, 0, P, 0, P, P)
+    assert st == tsv.TSV_ERR_UNSUPPORTED
+    st = lib.tsv_tree_verify_attn(P, P, P, P, P, P, P, 2, 8, 6, 4, 64, 16, 4, 8, 0.1, 0, P, 0, P, P)
+    assert st == tsv.TSV_ERR_ARG  # Hq not a multiple of Hkv
+    st = lib.tsv_kv_compact_accepted(P, P, P, P, P, P, P, 2, 8, 2, 64, 12, 4, 8, 0, P, P)
+    assert st == tsv.TSV_ERR_UNSUPPORTED  # block size 12
+    # empty batch is a no-op
+    assert lib.tsv_kv_compact_accepted(P, P, P, P, P, P, P, 0, 8, 2, 64, 16, 4, 8, 0, P, P) == tsv.TSV_OK
+    # single-chunk plans need no workspace
+    assert lib.tsv_attn_workspace_size(1, 15, 8, 2, 64, 16, 16, tsv.TSV_F32) == 0
+    assert lib.tsv_attn_workspace_size(1, 15, 8, 2, 64, 16, 17, tsv.TSV_F32) > 0  # prefix may need 2 chunks
+    assert lib.tsv_attn_workspace_size(1, 15, 8, 2, 96, 16, 17, tsv.TSV_F32) == 0

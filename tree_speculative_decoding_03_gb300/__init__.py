@@ -1,0 +1,142 @@
+"""Python binding of libtsv: the GB300 target-side verification step of tree-based
+speculative decoding (tree-masked paged attention, rejection-sampling tree walk,
+KV-cache compaction of the accepted path).
+
+Argument marshalling only: every step runs in the library's CUDA kernels.  Torch
+tensors supply device memory and the current CUDA stream.  There is no CPU
+fallback: if the library is not built, or the device cannot run it, calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+HEADER = os.path.join(os.path.dirname(HERE), "include", "tsv.h")
+
+TSV_OK, TSV_ERR_ARG, TSV_ERR_UNSUPPORTED, TSV_ERR_CUDA = 0, 1, 2, 3
+TSV_BF16, TSV_F32 = 0, 1
+DERR_PARENT, DERR_BLOCK, DERR_CAPACITY, DERR_TOKEN, DERR_NONFINITE = 1, 2, 4, 8, 16
+
+_lib = None
+
+
+class TsvError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"libtsv status {status}: {msg}")
+        self.status = status
+
+
+def lib_path() -> str:
+    from .build import LIB
+    return LIB
+
+
+def build(verbose: bool = False) -> str:
+    from .build import build_library
+    return build_library(verbose=verbose)
+
+
+def load():
+    """Loads the in-tree libtsv.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = lib_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"libtsv.so not built at {path}; run build() first")
+    lib = ctypes.CDLL(path)
+    P, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    lib.tsv_last_error.restype = ctypes.c_char_p
+    lib.tsv_last_error.argtypes = []
+    lib.tsv_attn_workspace_size.restype = sz
+    lib.tsv_attn_workspace_size.argtypes = [i32] * 8
+    lib.tsv_tree_verify_attn.restype = i32
+    lib.tsv_tree_verify_attn.argtypes = [P] * 7 + [i32] * 8 + [f32, i32, P, sz, P, P]
+    lib.tsv_tree_reject_sample.restype = i32
+    lib.tsv_tree_reject_sample.argtypes = [P, P, P, P, P, P, f32, i32, i32, i32, P, P, P, P, P, P]
+    lib.tsv_kv_compact_accepted.restype = i32
+    lib.tsv_kv_compact_accepted.argtypes = [P] * 7 + [i32] * 8 + [P, P]
+    _lib = lib
+    return lib
+
+
+def header_symbols() -> list:
+    """Entry points declared in include/tsv.h."""
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"\b(tsv_[a-z0-9_]+)\s*\(", text)))
+
+
+def _check(status: int):
+    if status != TSV_OK:
+        raise TsvError(status, load().tsv_last_error().decode())
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.bfloat16:
+        return TSV_BF16
+    if t.dtype == torch.float32:
+        return TSV_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _contig(*ts):
+    for t in ts:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def attn_workspace_size(B, N, Hq, Hkv, D, block_size, max_blocks, dtype_code) -> int:
+    return int(load().tsv_attn_workspace_size(B, N, Hq, Hkv, D, block_size, max_blocks, dtype_code))
+
+
+def tree_verify_attn(q, k_cache, v_cache, block_table, seq_lens, parent, out, scale: float,
+                     workspace=None, seq_err=None, stream=None):
+    """out[b,n,h,:] = tree-masked attention of q[b,n,h,:] over the paged cache
+    (see include/tsv.h).  q/out [B,N,Hq,D]; caches [num_blocks,bs,Hkv,D]."""
+    _contig(q, k_cache, v_cache, block_table, seq_lens, parent, out, workspace, seq_err)
+    B, N, Hq, D = q.shape
+    num_blocks, bs, Hkv, _ = k_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().tsv_tree_verify_attn(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(parent), _ptr(out),
+        B, N, Hq, Hkv, D, bs, block_table.shape[1], num_blocks, float(scale), _dtype_code(q),
+        _ptr(workspace), ws_bytes, _ptr(seq_err), _stream(stream)))
+
+
+def tree_reject_sample(target_logits, draft_probs, draft_tokens, parent, u_accept, u_bonus,
+                       temperature: float, accepted_nodes, accept_len, bonus_token, out_tokens, seq_err,
+                       stream=None):
+    """Rejection-sampling walk of the draft tree (see include/tsv.h)."""
+    _contig(target_logits, draft_probs, draft_tokens, parent, u_accept, u_bonus, accepted_nodes, accept_len,
+            bonus_token, out_tokens, seq_err)
+    B, N, V = target_logits.shape
+    _check(load().tsv_tree_reject_sample(
+        _ptr(target_logits), _ptr(draft_probs), _ptr(draft_tokens), _ptr(parent), _ptr(u_accept), _ptr(u_bonus),
+        float(temperature), B, N, V, _ptr(accepted_nodes), _ptr(accept_len), _ptr(bonus_token), _ptr(out_tokens),
+        _ptr(seq_err), _stream(stream)))
+
+
+def kv_compact_accepted(k_cache, v_cache, block_table, seq_lens, accepted_nodes, accept_len, new_seq_lens,
+                        seq_err, stream=None):
+    """Moves the accepted path's K/V rows into contiguous slots (see include/tsv.h)."""
+    _contig(k_cache, v_cache, block_table, seq_lens, accepted_nodes, accept_len, new_seq_lens, seq_err)
+    num_blocks, bs, Hkv, D = k_cache.shape
+    B, N = accepted_nodes.shape
+    _check(load().tsv_kv_compact_accepted(
+        _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(accepted_nodes), _ptr(accept_len),
+        _ptr(new_seq_lens), B, N, Hkv, D, bs, block_table.shape[1], num_blocks, _dtype_code(k_cache),
+        _ptr(seq_err), _stream(stream)))

@@ -1,0 +1,77 @@
+// attn_common.cuh -- launch plan and shared arguments of the tree-attention kernels.
+//
+// Work decomposition (both the fp32 FMA path and the bf16 tensor-core path):
+// one work item = (sequence b, kv head g, key chunk c, row group).  The rows of a
+// (b, g) pair are the R = N * Gq query rows (node n, head h = g*Gq + j) ordered
+// n-major, so one GQA group shares every K/V tile it loads.  The prefix of
+// sequence b is cut into nchunks(b) = max(1, ceil(L_b / chunk)) key chunks; the
+// last chunk also carries the N tree keys.  A sequence with one chunk writes its
+// output directly; otherwise each chunk writes (m, l, O/l) partials to the
+// workspace and the merge kernel combines them (log-sum-exp), one warp per row.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+namespace tsv {
+
+struct AttnPlan {
+    int G;             // query heads per kv head
+    int R;             // query rows per (b, kv head) = N * G
+    int rows_per_cta;  // rows one work item covers
+    int n_rgroups;     // ceil(R / rows_per_cta)
+    int chunk;         // prefix keys per chunk (multiple of 128)
+    int max_chunks;    // upper bound of nchunks(b) from the block-table capacity
+    size_t ws_bytes;   // partials workspace (0 when max_chunks == 1)
+};
+
+// Deterministic function of the shapes and the SM count (the workspace size query
+// and the call must agree).
+inline AttnPlan make_attn_plan(int B, int N, int Hq, int Hkv, int D, int block_size, int max_blocks,
+                               int rows_per_cta, int num_sms, int target_waves) {
+    AttnPlan p{};
+    p.G = Hq / Hkv;
+    p.R = N * p.G;
+    p.rows_per_cta = rows_per_cta;
+    p.n_rgroups = (p.R + rows_per_cta - 1) / rows_per_cta;
+    long long lmax = (long long)max_blocks * block_size - N;  // longest prefix the table can hold
+    if (lmax < 0) lmax = 0;
+    const long long units = (long long)B * Hkv * p.n_rgroups;
+    const long long target = (long long)num_sms * target_waves;
+    int chunk = 4096;
+    while (chunk > 256 && units * ((lmax + chunk - 1) / chunk) < target) chunk >>= 1;
+    p.chunk = chunk;
+    long long mc = (lmax + chunk - 1) / chunk;
+    p.max_chunks = (int)(mc < 1 ? 1 : mc);
+    if (p.max_chunks == 1) {
+        p.ws_bytes = 0;
+    } else {
+        const size_t rows = (size_t)B * Hkv * p.max_chunks * p.R;
+        p.ws_bytes = rows * (size_t)D * sizeof(float) + 2 * rows * sizeof(float);
+    }
+    return p;
+}
+
+struct AttnArgs {
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    const int32_t* parent;
+    void* out;
+    float* part_o;  // [B][Hkv][max_chunks][R][D]
+    float* part_m;  // [B][Hkv][max_chunks][R]
+    float* part_l;  // [B][Hkv][max_chunks][R]
+    int32_t* seq_err;
+    int B, N, Hq, Hkv, D;
+    int bs_log2, max_blocks, num_blocks;
+    float scale_log2;  // scale * log2(e)
+    int G, R, rows_per_cta, n_rgroups, chunk, max_chunks;
+};
+
+__host__ __device__ inline int num_chunks(int L, int chunk) {
+    return L <= 0 ? 1 : (L + chunk - 1) / chunk;
+}
+
+}  // namespace tsv

@@ -21,6 +21,8 @@ from __future__ import annotations
 
 import dataclasses
 import math
+import os
+from concurrent.futures import ThreadPoolExecutor
 from typing import Optional, Sequence
 
 import numpy as np
@@ -181,17 +183,42 @@ def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
     return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
+def _fill_normals(out: np.ndarray, seed: int, scale: float = 1.0, to_bf16: bool = False) -> None:
+    """Fills `out` (any shape, C order) with N(0, scale^2) draws.  The array is cut
+    into fixed slabs along axis 0; slab s draws from its own PCG64 stream seeded by
+    (seed, s), so the values do not depend on how many threads fill them."""
+    n0 = out.shape[0]
+    per_row = int(np.prod(out.shape[1:], dtype=np.int64)) if out.ndim > 1 else 1
+    rows = max(1, (1 << 22) // max(1, per_row))
+    slabs = [(s, min(n0, s + rows)) for s in range(0, n0, rows)]
+
+    def work(i):
+        lo, hi = slabs[i]
+        g = np.random.Generator(np.random.PCG64(np.random.SeedSequence([seed, i])))
+        x = g.standard_normal((hi - lo,) + out.shape[1:], dtype=np.float32)
+        if scale != 1.0:
+            x *= np.float32(scale)
+        out[lo:hi] = f32_to_bf16_bits(x) if to_bf16 else x
+
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
+        list(ex.map(work, range(len(slabs))))
+
+
 def _softmax_rows_f32(x: np.ndarray, T: float, chunk: int = 64) -> np.ndarray:
     """Draft-model distribution q = softmax(draft_logits / T), computed in float64 and
     stored as float32 (the draft model's output, an input to verification)."""
     flat = x.reshape(-1, x.shape[-1])
     out = np.empty_like(flat, dtype=np.float32)
-    for s in range(0, flat.shape[0], chunk):
+
+    def work(s):
         z = flat[s:s + chunk].astype(np.float64) / T
         z -= z.max(axis=1, keepdims=True)
         np.exp(z, out=z)
         z /= z.sum(axis=1, keepdims=True)
         out[s:s + chunk] = z
+
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
+        list(ex.map(work, range(0, flat.shape[0], chunk)))
     return out.reshape(x.shape)
 
 
@@ -244,25 +271,25 @@ def generate(w: Workload, *, seed: Optional[int] = None, temperature: Optional[f
         block_table[b, :nblk[b]] = perm[off:off + nblk[b]]
         off += int(nblk[b])
 
-    # 4. q / k / v ~ N(0, 1)
+    # 4. q / k / v ~ N(0, 1) (the caches are filled slab-parallel from one drawn seed)
     def normals(shape):
         return rng.standard_normal(shape, dtype=np.float32)
 
     q = normals((B, N, w.Hq, w.D))
+    kv_seed = int(rng.integers(0, 2**63 - 1))
     cache_shape = (num_blocks, bs, w.Hkv, w.D)
     if w.dtype == "bf16":
         q = f32_to_bf16_bits(q)
         k_cache = np.empty(cache_shape, dtype=np.uint16)
         v_cache = np.empty(cache_shape, dtype=np.uint16)
-        slab = max(1, (1 << 24) // (bs * w.Hkv * w.D))
-        for dst in (k_cache, v_cache):
-            for s in range(0, num_blocks, slab):
-                e = min(num_blocks, s + slab)
-                dst[s:e] = f32_to_bf16_bits(normals((e - s,) + cache_shape[1:]))
+        _fill_normals(k_cache, kv_seed * 2 % (2**63), to_bf16=True)
+        _fill_normals(v_cache, (kv_seed * 2 + 1) % (2**63), to_bf16=True)
         nan_val = BF16_NAN
     elif w.dtype == "f32":
-        k_cache = normals(cache_shape)
-        v_cache = normals(cache_shape)
+        k_cache = np.empty(cache_shape, dtype=np.float32)
+        v_cache = np.empty(cache_shape, dtype=np.float32)
+        _fill_normals(k_cache, kv_seed * 2 % (2**63))
+        _fill_normals(v_cache, (kv_seed * 2 + 1) % (2**63))
         nan_val = np.float32(np.nan)
     else:
         raise ValueError(w.dtype)
@@ -274,13 +301,13 @@ def generate(w: Workload, *, seed: Optional[int] = None, temperature: Optional[f
                 v_cache[blk, t % bs] = nan_val
 
     # 5. draft logits 2*N(0,1) and the draft distribution q = softmax(draft / T)
-    draft_logits = normals((B, N, V))
-    draft_logits *= np.float32(2.0)
+    draft_logits = np.empty((B, N, V), dtype=np.float32)
+    _fill_normals(draft_logits, int(rng.integers(0, 2**63 - 1)), scale=2.0)
     draft_probs = _softmax_rows_f32(draft_logits, T if T > 0 else 1.0)
 
     # 6. target logits = draft + N(0, noise^2); a seeded subset gets target == draft
-    target_logits = normals((B, N, V))
-    target_logits *= np.float32(w.noise)
+    target_logits = np.empty((B, N, V), dtype=np.float32)
+    _fill_normals(target_logits, int(rng.integers(0, 2**63 - 1)), scale=w.noise)
     target_logits += draft_logits
     pq_seqs = np.zeros(0, dtype=np.int64)
     if w.pq_frac > 0:
@@ -308,7 +335,8 @@ def generate(w: Workload, *, seed: Optional[int] = None, temperature: Optional[f
                 key = np.log(draft_probs[b, i].astype(np.float64)) + rng.gumbel(size=V)
             else:
                 key = draft_logits[b, i].astype(np.float64)
-            top = np.argsort(-key, kind="stable")[:k]
+            cand = np.argpartition(-key, k - 1)[:k] if k < V else np.arange(V)
+            top = cand[np.lexsort((cand, -key[cand]))]  # descending key, ties to the lower id
             draft_tokens[b, kids[i]] = top
 
     # 8. uniforms U[0, 1)
