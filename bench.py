@@ -134,6 +134,25 @@ class ClockSampler:
                 "samples": len(rows), "reasons": sorted(reasons)}
 
 
+# ----------------------------------------------------------------------------- multi-process plumbing
+
+def reduce_max(x: float, world: int) -> float:
+    """Max over ranks (the slowest replica sets the whole-job time)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, seconds: float, world: int) -> float:
+    """Units processed by all ranks divided by the slowest rank's time."""
+    return world * units_per_rank / reduce_max(seconds, world)
+
+
 # ----------------------------------------------------------------------------- algorithmic work
 
 def attn_bytes(inp):
@@ -297,12 +316,8 @@ def run_ours(args, rank, world, local_rank):
     per = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in evs])  # ms
     step_ms = per.sum(axis=1)
     dev_s = float(step_ms.sum()) / 1e3
-    if world > 1:
-        t = torch.tensor([dev_s], device="cuda", dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        dev_s = float(t.item())
     tokens_per_step = B * N
-    value = world * tokens_per_step * K / dev_s
+    value = whole_job_rate(tokens_per_step * K, dev_s, world)
 
     # decisions of the last step, for the verifier's realised bytes
     an, al = acc_nodes.cpu().numpy(), acc_len.cpu().numpy()
@@ -341,11 +356,7 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     barrier()
     e2e_s = e0.elapsed_time(e1) / 1e3
-    if world > 1:
-        t = torch.tensor([e2e_s], device="cuda", dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
-    e2e = {"value": world * tokens_per_step * K / e2e_s, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+    e2e = {"value": whole_job_rate(tokens_per_step * K, e2e_s, world), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
            "d2h_bytes_per_step": int(d2h)}
 
     launches_per_step = 3 + (1 if ws_bytes else 0)

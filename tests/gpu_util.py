@@ -18,22 +18,25 @@ def dev(x, dtype=None):
     return t.cuda()
 
 
-def device_inputs(inp):
-    bf = inp["dtype"] == "bf16"
-    el = torch.bfloat16 if bf else None
+def device_inputs(inp, attn=True, verify=True):
+    d = dict(parent=dev(inp["parent"]))
+    if attn:
+        bf = inp["dtype"] == "bf16"
+        el = torch.bfloat16 if bf else None
 
-    def kv(x):
-        return dev(x.view(np.int16) if bf else x, el)
+        def kv(x):
+            return dev(x.view(np.int16) if bf else x, el)
 
-    d = dict(q=kv(inp["q"]), k_cache=kv(inp["k_cache"]), v_cache=kv(inp["v_cache"]),
-             block_table=dev(inp["block_table"]), seq_lens=dev(inp["seq_lens"]), parent=dev(inp["parent"]),
-             target_logits=dev(inp["target_logits"]), draft_probs=dev(inp["draft_probs"]),
-             draft_tokens=dev(inp["draft_tokens"]), u_accept=dev(inp["u_accept"]), u_bonus=dev(inp["u_bonus"]))
+        d.update(q=kv(inp["q"]), k_cache=kv(inp["k_cache"]), v_cache=kv(inp["v_cache"]),
+                 block_table=dev(inp["block_table"]), seq_lens=dev(inp["seq_lens"]))
+    if verify:
+        d.update(target_logits=dev(inp["target_logits"]), draft_probs=dev(inp["draft_probs"]),
+                 draft_tokens=dev(inp["draft_tokens"]), u_accept=dev(inp["u_accept"]), u_bonus=dev(inp["u_bonus"]))
     return d
 
 
 def run_attn(inp, d=None):
-    d = d or device_inputs(inp)
+    d = d or device_inputs(inp, verify=False)
     B, N, Hq, D = d["q"].shape
     out = torch.empty_like(d["q"])
     ws_bytes = tsv.attn_workspace_size(B, N, Hq, inp["Hkv"], D, inp["block_size"], inp["max_blocks"],
@@ -47,7 +50,7 @@ def run_attn(inp, d=None):
 
 
 def run_verify(inp, d=None, temperature=None):
-    d = d or device_inputs(inp)
+    d = d or device_inputs(inp, attn=False)
     B, N, V = d["target_logits"].shape
     T = inp["T"] if temperature is None else temperature
     an = torch.full((B, N), -9, dtype=torch.int32, device="cuda")
@@ -63,7 +66,7 @@ def run_verify(inp, d=None, temperature=None):
 
 
 def run_compact(inp, accepted_nodes, accept_len, d=None):
-    d = d or device_inputs(inp)
+    d = d or device_inputs(inp, verify=False)
     B = len(accept_len)
     new_len = torch.full((B,), -9, dtype=torch.int32, device="cuda")
     err = torch.full((B,), -9, dtype=torch.int32, device="cuda")

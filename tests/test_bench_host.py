@@ -1,0 +1,38 @@
+"""Host-side logic of bench.py: algorithmic byte counts and the replica aggregation
+(max over ranks) with world_size 2 over gloo."""
+import os
+
+import numpy as np
+import torch.multiprocessing as mp
+
+import bench
+import workloads as W
+
+
+def test_algorithmic_bytes():
+    inp = W.generate(W.CONFIGS[1].replace(B=2, V=64))
+    # K and V of 2054 slots x 8 heads x 128 dims x 2 bytes, both sequences; Q in and O out
+    assert bench.attn_bytes(inp) == 2 * 2054 * 8 * 128 * 2 * 2 + 2 * 2 * 6 * 32 * 128 * 2
+    an = np.array([[0, 1, 2, -1, -1, -1], [0, -1, -1, -1, -1, -1]])
+    al = np.array([2, 0])
+    # seq 0 visits 3 nodes; first children accepted at 0 and 1; node 2 rejects its child -> draft row read
+    # seq 1 visits the root and rejects its only child -> draft row read
+    assert bench.verify_bytes(inp, an, al) == (3 + 1 + 1 + 1) * 64 * 4
+    assert bench.compact_bytes(inp, al) == 2 * 8 * 128 * 2 * 2 * 2
+
+
+def _worker(rank, world, port, out):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    secs = [0.5, 2.0][rank]
+    out[rank] = bench.whole_job_rate(100.0, secs, world)
+    dist.destroy_process_group()
+
+
+def test_replica_rate_uses_slowest_rank():
+    mgr = mp.Manager()
+    out = mgr.dict()
+    port = 29500 + os.getpid() % 1000
+    mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
+    assert out[0] == out[1] == 2 * 100.0 / 2.0

@@ -11,7 +11,7 @@ cudaError_t launch_kv_compact(void* k_cache, void* v_cache, const int32_t* block
                               const int32_t* accepted_nodes, const int32_t* accept_len, int32_t* new_seq_lens,
                               int B, int N, int Hkv, int D, int block_size, int max_blocks, int num_blocks,
                               int elem_bytes, int32_t* seq_err, cudaStream_t stream);
-cudaError_t launch_attn_simt(const AttnArgs& a, bool bf16, cudaStream_t stream);
+cudaError_t launch_attn_simt_f32(const AttnArgs& a, cudaStream_t stream);
 cudaError_t launch_attn_merge(const AttnArgs& a, bool bf16, cudaStream_t stream);
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t stream);
 bool attn_tc_supported(int D);
@@ -53,7 +53,7 @@ int log2i(int x) {
     return l;
 }
 
-bool use_tc(tsv_dtype dt, int D) { return dt == TSV_BF16 && tsv::attn_tc_supported(D); }
+bool use_tc(tsv_dtype dt, int D) { return dt == TSV_BF16 && tsv::attn_tc_supported(D); }  // D checked before
 
 tsv::AttnPlan plan_for(int B, int N, int Hq, int Hkv, int D, int block_size, int max_blocks, tsv_dtype dt) {
     const bool tc = use_tc(dt, D);
@@ -135,12 +135,12 @@ tsv_status tsv_tree_verify_attn(const void* q, const void* k_cache, const void* 
     a.max_chunks = p.max_chunks;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (use_tc(dtype, D)) {
+    if (dtype == TSV_BF16) {
         e = tsv::launch_attn_tc(a, s);
-        if (e == cudaSuccess) e = tsv::launch_attn_merge(a, true, s);
     } else {
-        e = tsv::launch_attn_simt(a, dtype == TSV_BF16, s);
+        e = tsv::launch_attn_simt_f32(a, s);
     }
+    if (e == cudaSuccess) e = tsv::launch_attn_merge(a, dtype == TSV_BF16, s);
     if (e != cudaSuccess) return cuda_fail(e, "tree_verify_attn launch");
     return TSV_OK;
 }

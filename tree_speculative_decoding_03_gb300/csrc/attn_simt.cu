@@ -1,5 +1,5 @@
 // attn_simt.cu -- tree-masked attention on the FMA pipes (fp32 inputs), and the
-// split-K merge shared with the tensor-core path.
+// split-K merge shared with the tensor-core path (bf16 inputs).
 //
 // sglang report, "What is Tree-Attention?" and "Tree-based Speculative Decoding
 // (EAGLE) Implementation Summary": the flattened tree's tokens are scored in one
@@ -219,21 +219,16 @@ __global__ void __launch_bounds__(256) attn_merge_kernel(const AttnArgs a) {
     for (int j = 0; j < DP; ++j) out[row * D + lane + 32 * j] = from_f32<T>(acc[j] * inv);
 }
 
-template <typename T, int D>
+template <int D>
 static cudaError_t launch_simt_inst(const AttnArgs& a, cudaStream_t stream) {
     dim3 grid((unsigned)(a.n_rgroups * a.max_chunks), (unsigned)a.Hkv, (unsigned)a.B);
-    attn_simt_kernel<T, D><<<grid, kSimtThreads, 0, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess || a.max_chunks == 1) return e;
-    const long long rows = (long long)a.B * a.N * a.Hq;
-    attn_merge_kernel<T, D><<<(unsigned)((rows + 7) / 8), 256, 0, stream>>>(a);
+    attn_simt_kernel<float, D><<<grid, kSimtThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
-cudaError_t launch_attn_simt(const AttnArgs& a, bool bf16, cudaStream_t stream) {
-    if (bf16) return a.D == 64 ? launch_simt_inst<__nv_bfloat16, 64>(a, stream)
-                               : launch_simt_inst<__nv_bfloat16, 128>(a, stream);
-    return a.D == 64 ? launch_simt_inst<float, 64>(a, stream) : launch_simt_inst<float, 128>(a, stream);
+// fp32 inputs only: bf16 runs on the tensor-core kernel (attn_tc.cu)
+cudaError_t launch_attn_simt_f32(const AttnArgs& a, cudaStream_t stream) {
+    return a.D == 64 ? launch_simt_inst<64>(a, stream) : launch_simt_inst<128>(a, stream);
 }
 
 template <typename T, int D>
