@@ -74,22 +74,3 @@ def test_full_size_sampled_rows(cfg):
     err = np.abs(got[rows] - want).max()
     assert err <= TOL[inp["dtype"]], err
 
-
-def test_bf16_runs_on_the_tensor_core_kernel():
-    """The bf16 path launches the tcgen05 kernel (and the merge for split prefixes);
-    fp32 launches the FMA kernel.  Kernel names come from the CUDA profiler."""
-    import torch
-    from torch.profiler import ProfilerActivity, profile
-
-    names = {}
-    for dtype in ("bf16", "f32"):
-        inp = W.generate(W.CONFIGS[1].replace(B=2, Hq=8, Hkv=2, dtype=dtype, prefix=(3000, 3000), V=64, seed=1))
-        run_attn(inp)  # warm
-        with profile(activities=[ProfilerActivity.CUDA]) as prof:
-            run_attn(inp)
-            torch.cuda.synchronize()
-        names[dtype] = {e.name for e in prof.events() if e.device_type.name == "CUDA"}
-    assert any("attn_tc_kernel" in n for n in names["bf16"]), names["bf16"]
-    assert any("attn_merge_kernel" in n for n in names["bf16"])
-    assert not any("attn_simt_kernel" in n for n in names["bf16"])
-    assert any("attn_simt_kernel" in n for n in names["f32"]), names["f32"]
