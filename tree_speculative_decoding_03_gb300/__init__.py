@@ -30,12 +30,12 @@ class TsvError(RuntimeError):
 
 
 def lib_path() -> str:
-    from .build import LIB
+    from .builder import LIB
     return LIB
 
 
 def build(verbose: bool = False) -> str:
-    from .build import build_library
+    from .builder import build_library
     return build_library(verbose=verbose)
 
 
