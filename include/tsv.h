@@ -103,6 +103,34 @@ tsv_status tsv_tree_verify_attn(const void *q, const void *k_cache, const void *
                                 int32_t *seq_err, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * tsv_tree_verify_attn without a caller workspace (the pages have no counterpart
+ * of this call; it is an interface convenience).
+ *
+ * For callers that cannot allocate device memory -- e.g. a plugin inside an engine
+ * that owns all device memory and passes only inputs and outputs, or a loop that
+ * must not call cudaMalloc because it can synchronise the device.  Same arguments
+ * and result as tsv_tree_verify_attn, minus the workspace: the split-K partials go
+ * to a scratch array of tsv_noalloc_scratch_bytes() (32 MiB) that the library
+ * defines in device memory; every GPU that loads the library holds it until the
+ * process exits.  Nothing is allocated per call.
+ *  - Shapes whose tsv_attn_workspace_size exceeds the array are rejected with
+ *    TSV_ERR_UNSUPPORTED before anything is launched.
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any stream
+ *    capture.
+ *  - All calls share the array: calls that overlap on the GPU race on it and must
+ *    be ordered by the caller.  Each call rewrites every scratch byte it reads.
+ * ------------------------------------------------------------------------- */
+size_t tsv_noalloc_scratch_bytes(void);
+
+tsv_status tsv_tree_verify_attn_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                        const int32_t *block_table, const int32_t *seq_lens,
+                                        const int32_t *parent, void *out, int B, int N, int Hq,
+                                        int Hkv, int D, int block_size, int max_blocks,
+                                        int num_blocks, float scale, tsv_dtype dtype,
+                                        int32_t *seq_err, void *stream);
+
+/* ---------------------------------------------------------------------------
  * Rejection-sampling verification of the tree (statistical-learning-notes ch.07
  * "Speculative Decoding", section "Draft Token Validation"; Sequoia summary,
  * sections "Scalable Speculative Decoding" and "Robust Sampling").

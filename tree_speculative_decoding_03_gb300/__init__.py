@@ -57,6 +57,10 @@ def load():
     lib.tsv_tree_verify_attn.argtypes = [P] * 7 + [i32] * 8 + [f32, i32, P, sz, P, P]
     lib.tsv_tree_reject_sample.restype = i32
     lib.tsv_tree_reject_sample.argtypes = [P, P, P, P, P, P, f32, i32, i32, i32, P, P, P, P, P, P]
+    lib.tsv_tree_verify_attn_noalloc.restype = i32
+    lib.tsv_tree_verify_attn_noalloc.argtypes = [P] * 7 + [i32] * 8 + [f32, i32, P, P]
+    lib.tsv_noalloc_scratch_bytes.restype = sz
+    lib.tsv_noalloc_scratch_bytes.argtypes = []
     lib.tsv_kv_compact_accepted.restype = i32
     lib.tsv_kv_compact_accepted.argtypes = [P] * 7 + [i32] * 8 + [P, P]
     _lib = lib
@@ -115,6 +119,19 @@ def tree_verify_attn(q, k_cache, v_cache, block_table, seq_lens, parent, out, sc
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(parent), _ptr(out),
         B, N, Hq, Hkv, D, bs, block_table.shape[1], num_blocks, float(scale), _dtype_code(q),
         _ptr(workspace), ws_bytes, _ptr(seq_err), _stream(stream)))
+
+
+def tree_verify_attn_noalloc(q, k_cache, v_cache, block_table, seq_lens, parent, out, scale: float,
+                             seq_err, stream=None):
+    """tree_verify_attn for callers that cannot allocate: the split-K scratch is the
+    library's own fixed device array (see include/tsv.h; calls must not overlap)."""
+    _contig(q, k_cache, v_cache, block_table, seq_lens, parent, out, seq_err)
+    B, N, Hq, D = q.shape
+    num_blocks, bs, Hkv, _ = k_cache.shape
+    _check(load().tsv_tree_verify_attn_noalloc(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(parent), _ptr(out),
+        B, N, Hq, Hkv, D, bs, block_table.shape[1], num_blocks, float(scale), _dtype_code(q),
+        _ptr(seq_err), _stream(stream)))
 
 
 def tree_reject_sample(target_logits, draft_probs, draft_tokens, parent, u_accept, u_bonus,

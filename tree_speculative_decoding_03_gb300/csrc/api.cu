@@ -77,6 +77,17 @@ tsv_status check_attn_shapes(int B, int N, int Hq, int Hkv, int D, int block_siz
 
 }  // namespace
 
+namespace tsv {
+// Records a failure message for tsv_last_error() from other translation units.
+tsv_status report_error(tsv_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return s;
+}
+}  // namespace tsv
+
 extern "C" {
 
 const char* tsv_last_error(void) { return g_err; }
