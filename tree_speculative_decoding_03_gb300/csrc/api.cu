@@ -57,8 +57,10 @@ bool use_tc(tsv_dtype dt, int D) { return dt == TSV_BF16 && tsv::attn_tc_support
 
 tsv::AttnPlan plan_for(int B, int N, int Hq, int Hkv, int D, int block_size, int max_blocks, tsv_dtype dt) {
     const bool tc = use_tc(dt, D);
+    // tensor-core work items hold a whole SM (TMEM, ~226 KB smem): about two waves of
+    // chunks of at least 512 keys; FMA items are small: eight waves of chunks >= 256
     return tsv::make_attn_plan(B, N, Hq, Hkv, D, block_size, max_blocks,
-                               tc ? tsv::attn_tc_rows_per_cta() : 16, device_sms(), tc ? 4 : 8);
+                               tc ? tsv::attn_tc_rows_per_cta() : 16, device_sms(), tc ? 2 : 8, tc ? 512 : 256);
 }
 
 tsv_status check_attn_shapes(int B, int N, int Hq, int Hkv, int D, int block_size, int max_blocks,

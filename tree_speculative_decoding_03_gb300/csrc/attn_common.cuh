@@ -28,7 +28,7 @@ struct AttnPlan {
 // Deterministic function of the shapes and the SM count (the workspace size query
 // and the call must agree).
 inline AttnPlan make_attn_plan(int B, int N, int Hq, int Hkv, int D, int block_size, int max_blocks,
-                               int rows_per_cta, int num_sms, int target_waves) {
+                               int rows_per_cta, int num_sms, int target_waves, int min_chunk) {
     AttnPlan p{};
     p.G = Hq / Hkv;
     p.R = N * p.G;
@@ -39,7 +39,7 @@ inline AttnPlan make_attn_plan(int B, int N, int Hq, int Hkv, int D, int block_s
     const long long units = (long long)B * Hkv * p.n_rgroups;
     const long long target = (long long)num_sms * target_waves;
     int chunk = 4096;
-    while (chunk > 256 && units * ((lmax + chunk - 1) / chunk) < target) chunk >>= 1;
+    while (chunk > min_chunk && units * ((lmax + chunk - 1) / chunk) < target) chunk >>= 1;
     p.chunk = chunk;
     long long mc = (lmax + chunk - 1) / chunk;
     p.max_chunks = (int)(mc < 1 ? 1 : mc);

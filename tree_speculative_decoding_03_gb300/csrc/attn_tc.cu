@@ -171,6 +171,18 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// key t of the work item's range is visible to a row whose root-to-node path is the
+// bit set anc: every prefix key (t < L) below the range end, and the tree key L + j iff
+// node j is on the path
+__device__ __forceinline__ bool key_visible(int t, int k_end, int L, uint32_t anc0, uint32_t anc1, uint32_t anc2,
+                                            uint32_t anc3) {
+    if (t >= k_end) return false;
+    if (t < L) return true;
+    const int jn = t - L;
+    const uint32_t w = jn < 64 ? (jn < 32 ? anc0 : anc1) : (jn < 96 ? anc2 : anc3);
+    return (w >> (jn & 31)) & 1u;
+}
+
 // byte offset of 16-byte chunk `q` (along the contiguous dimension) of row `row` in a
 // tile stored as 64-element halves of [128 rows x 128 B], 128B-swizzled
 __device__ __forceinline__ uint32_t sw128_offset(int row, int q) {
@@ -233,7 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + lay.bars + 8 * Bars::kCount);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + lay.bars + 8 * Bars::kCount + 4);
     int* s_flag = reinterpret_cast<int*>(smem + lay.bars + 8 * Bars::kCount + 8);
-    auto bar = [&](int i) { return smem_u32(&bars[i]); };
+    const uint32_t bar0 = smem_u32(bars);
+    auto bar = [=](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int b = blockIdx.z, g = blockIdx.y;
@@ -315,30 +328,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     int my_err = 0;
 
     if (warp == 0) {
-        // ============================ TMA producer
-        if (lane == 0) {
-            const int nfills = 2 * ntiles;
-            for (int f = 0; f < nfills && !my_err; ++f) {
-                const int slot = f % nslots, use = f / nslots;
-                if (use > 0 && !mbar_wait(bar(Bars::kEmpty + slot), (use - 1) & 1, s_abort)) {
-                    my_err = 1;
-                    break;
-                }
-                const int t0 = k_begin + (f >> 1) * kTileKeys;
-                const int t1 = min(t0 + kTileKeys, k_end);
-                const int nblk = (t1 - t0 + bs - 1) >> a.bs_log2;
-                const CUtensorMap* map = (f & 1) ? &tmv : &tmk;
-                const uint32_t dst = smem_u32(smem + lay.ring + slot * SLOT);
-                mbar_expect_tx(bar(Bars::kFull + slot), static_cast<uint32_t>(nblk * bs * 128 * HALVES));
-                for (int jb = 0; jb < nblk; ++jb) {
-                    const int blk = bt[(t0 >> a.bs_log2) + jb];
-#pragma unroll
-                    for (int hh = 0; hh < HALVES; ++hh)
-                        tma_load_3d(dst + hh * kHalfBytes + jb * bs * 128, map, bar(Bars::kFull + slot), hh * 64, g,
-                                    blk * bs);
-                }
+        // ============================ TMA producer (whole warp: lane j loads the id of
+        // the tile's j-th cache block and issues that block's boxes, so a tile's block
+        // ids are fetched in one coalesced load instead of one dependent load each)
+        const int nfills = 2 * ntiles;
+        for (int f = 0; f < nfills && !my_err; ++f) {
+            const int slot = f % nslots, use = f / nslots;
+            if (use > 0 && !__all_sync(0xffffffffu, mbar_wait(bar(Bars::kEmpty + slot), (use - 1) & 1, s_abort))) {
+                my_err = 1;
+                break;
             }
-            // never leave with copies in flight: wait for the latest fill of every slot
+            const int t0 = k_begin + (f >> 1) * kTileKeys;
+            const int t1 = min(t0 + kTileKeys, k_end);
+            const int nblk = (t1 - t0 + bs - 1) >> a.bs_log2;
+            const CUtensorMap* map = (f & 1) ? &tmv : &tmk;
+            const uint32_t dst = smem_u32(smem + lay.ring + slot * SLOT);
+            if (lane == 0) mbar_expect_tx(bar(Bars::kFull + slot), static_cast<uint32_t>(nblk * bs * 128 * HALVES));
+            __syncwarp();
+            for (int jb = lane; jb < nblk; jb += 32) {
+                const int blk = bt[(t0 >> a.bs_log2) + jb];
+#pragma unroll
+                for (int hh = 0; hh < HALVES; ++hh)
+                    tma_load_3d(dst + hh * kHalfBytes + jb * bs * 128, map, bar(Bars::kFull + slot), hh * 64, g,
+                                blk * bs);
+            }
+        }
+        // never leave with copies in flight: wait for the latest fill of every slot
+        if (lane == 0) {
             for (int f = max(0, 2 * ntiles - nslots); f < 2 * ntiles; ++f) {
                 volatile int never = 0;
                 if (!mbar_wait(bar(Bars::kFull + f % nslots), (f / nslots) & 1, &never)) my_err = 1;
@@ -349,9 +365,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16(128, 128, false);
             constexpr uint32_t idO = idesc_bf16(128, D, true);
-            auto issue_S = [&](int m, int slot) {
-                const uint32_t qa = smem_u32(smem + lay.q0) + m * (128u * D * 2u);
-                const uint32_t kb = smem_u32(smem + lay.ring + slot * SLOT);
+            const uint32_t q_base = smem_u32(smem + lay.q0), p_base = smem_u32(smem + lay.p0);
+            const uint32_t ring_base = smem_u32(smem + lay.ring);
+            auto issue_S = [=](int m, int slot) {
+                const uint32_t qa = q_base + m * (128u * D * 2u);
+                const uint32_t kb = ring_base + slot * SLOT;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
@@ -359,9 +377,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                              k > 0);
                 }
             };
-            auto issue_PV = [&](int m, int slot, bool acc_first) {
-                const uint32_t pa = smem_u32(smem + lay.p0) + m * kPBytes;
-                const uint32_t vb = smem_u32(smem + lay.ring + slot * SLOT);
+            auto issue_PV = [=](int m, int slot, bool acc_first) {
+                const uint32_t pa = p_base + m * kPBytes;
+                const uint32_t vb = ring_base + slot * SLOT;
 #pragma unroll
                 for (int k = 0; k < kTileKeys / 16; ++k) {
                     const uint32_t aoff = (k >> 2) * kHalfBytes + (k & 3) * 32;
@@ -414,9 +432,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp >= 4) {
         // ============================ softmax warpgroups
         const int wg = (warp - 4) >> 2;
-        const int tw = tid - 128 - wg * 128;  // TMEM lane = row within the M tile
-        const int r = r_base + wg * 128 + tw;
-        const bool valid = (wg < nm) && (r < a.R);
+        const int tw = tid - 128 - wg * 128;  // TMEM lane = tile row handled by this thread
+        // A partial M tile deals its rows round-robin over the four 32-lane quadrants of
+        // TMEM (tile row tw holds row 4*(tw%32) + tw/32), so all four softmax warps share
+        // the work; a full tile keeps the identity order.
+        const int rows_here = min(128, a.R - r_base - wg * 128);
+        const int rl = rows_here < 128 ? 4 * (tw & 31) + (tw >> 5) : tw;
+        const int r = r_base + wg * 128 + rl;
+        const bool valid = (wg < nm) && (rl < rows_here);
         const int n = valid ? r / a.G : 0;
         const int h = g * a.G + (valid ? r % a.G : 0);
         // Q row -> swizzled shared tile
@@ -435,11 +458,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_arrive(bar(Bars::kQ));
         }
         // ancestor mask of this row's node (tree keys only)
-        uint32_t anc[4] = {0u, 0u, 0u, 0u};
+        uint32_t anc0 = 0u, anc1 = 0u, anc2 = 0u, anc3 = 0u;
         if (valid && has_tree) {
             int x = n;
             for (int step = 0; step <= N && x >= 0 && x < N; ++step) {
-                anc[x >> 5] |= 1u << (x & 31);
+                const uint32_t bit = 1u << (x & 31);
+                const int w = x >> 5;
+                anc0 |= w == 0 ? bit : 0u;
+                anc1 |= w == 1 ? bit : 0u;
+                anc2 |= w == 2 ? bit : 0u;
+                anc3 |= w == 3 ? bit : 0u;
                 x = s_par[x];
             }
         }
@@ -457,32 +485,43 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
             tc_fence_after();
             if (warp_active) {
-                // Two passes over the S row in TMEM (32 columns at a time): the masked
-                // max first, then P = 2^(s - m) written as bf16 into the swizzled P tile.
-                // Re-reading TMEM is cheaper than holding 128 scores in registers.
+                // Two passes over the S row in TMEM, 64 columns per wait: the raw max
+                // first, then P = 2^(s*scale - m) written as bf16 into the swizzled P
+                // tile.  Independent accumulators (8 for the max, 4 for the sum) keep the
+                // FMNMX/MUFU latency chains short; the masked path is taken only for
+                // tiles that reach past the prefix.
                 const bool full_tile = (t0 + kTileKeys <= L) && (t0 + kTileKeys <= k_end);
-                auto masked = [&](uint32_t bits, int cc) -> float {
-                    const float x = __uint_as_float(bits) * sl2;
-                    if (full_tile) return x;
-                    const int t = t0 + cc;
-                    bool vis = t < k_end;
-                    if (vis && t >= L) {
-                        const int jn = t - L;
-                        vis = (anc[jn >> 5] >> (jn & 31)) & 1u;
-                    }
-                    return vis ? x : -INFINITY;
-                };
-                float mx = -INFINITY;
+                float mxa[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) mxa[i] = -INFINITY;
 #pragma unroll 1
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t part[32];
-                    tmem_ld32(tS + q4 * 32, part);
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    uint32_t pa[32], pb[32];
+                    tmem_ld32(tS + h2 * 64, pa);
+                    tmem_ld32(tS + h2 * 64 + 32, pb);
                     tmem_wait_ld();
                     if (valid) {
+                        if (full_tile) {
 #pragma unroll
-                        for (int cc = 0; cc < 32; ++cc) mx = fmaxf(mx, masked(part[cc], q4 * 32 + cc));
+                            for (int cc = 0; cc < 32; ++cc) {
+                                mxa[cc & 7] = fmaxf(mxa[cc & 7], __uint_as_float(pa[cc]));
+                                mxa[cc & 7] = fmaxf(mxa[cc & 7], __uint_as_float(pb[cc]));
+                            }
+                        } else {
+#pragma unroll
+                            for (int cc = 0; cc < 32; ++cc) {
+                                const int c0 = h2 * 64 + cc;
+                                if (key_visible(t0 + c0, k_end, L, anc0, anc1, anc2, anc3))
+                                    mxa[cc & 7] = fmaxf(mxa[cc & 7], __uint_as_float(pa[cc]));
+                                if (key_visible(t0 + c0 + 32, k_end, L, anc0, anc1, anc2, anc3))
+                                    mxa[cc & 7] = fmaxf(mxa[cc & 7], __uint_as_float(pb[cc]));
+                            }
+                        }
                     }
                 }
+                const float mx_raw = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
+                                           fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
+                const float mx = mx_raw * sl2;  // scale > 0: max commutes with it
                 // the PV product of the previous tile must be done before O or P change
                 if (j > 0) {
                     ok = __all_sync(0xffffffffu, mbar_wait(bar(Bars::kO + wg), (j - 1) & 1, s_abort));
@@ -512,26 +551,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_wait_st();
                 }
                 const bool live = valid && m_run != -INFINITY;
+                const float neg_m = -m_run;
+                float la[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll 1
-                for (int q4 = 0; q4 < 4; ++q4) {
-                    uint32_t part[32];
-                    tmem_ld32(tS + q4 * 32, part);
+                for (int h2 = 0; h2 < 2; ++h2) {
+                    uint32_t pa[32], pb[32];
+                    tmem_ld32(tS + h2 * 64, pa);
+                    tmem_ld32(tS + h2 * 64 + 32, pb);
                     tmem_wait_ld();
+                    // P in place of the scores (as bit patterns): pa = columns 0..31, pb = 32..63
+                    if (live && full_tile) {
 #pragma unroll
-                    for (int q8 = 0; q8 < 4; ++q8) {
+                        for (int cc = 0; cc < 32; ++cc) {
+                            pa[cc] = __float_as_uint(ex2(fmaf(__uint_as_float(pa[cc]), sl2, neg_m)));
+                            pb[cc] = __float_as_uint(ex2(fmaf(__uint_as_float(pb[cc]), sl2, neg_m)));
+                        }
+                    } else if (live) {
+#pragma unroll
+                        for (int cc = 0; cc < 32; ++cc) {
+                            const int c0 = h2 * 64 + cc;
+                            pa[cc] = key_visible(t0 + c0, k_end, L, anc0, anc1, anc2, anc3)
+                                         ? __float_as_uint(ex2(fmaf(__uint_as_float(pa[cc]), sl2, neg_m)))
+                                         : 0u;
+                            pb[cc] = key_visible(t0 + c0 + 32, k_end, L, anc0, anc1, anc2, anc3)
+                                         ? __float_as_uint(ex2(fmaf(__uint_as_float(pb[cc]), sl2, neg_m)))
+                                         : 0u;
+                        }
+                    } else {
+#pragma unroll
+                        for (int cc = 0; cc < 32; ++cc) pa[cc] = pb[cc] = 0u;
+                    }
+#pragma unroll
+                    for (int q8 = 0; q8 < 8; ++q8) {
                         uint32_t w[4];
 #pragma unroll
                         for (int e2 = 0; e2 < 4; ++e2) {
-                            const int cc = q8 * 8 + 2 * e2;
-                            const float p0 = live ? ex2(masked(part[cc], q4 * 32 + cc) - m_run) : 0.0f;
-                            const float p1 = live ? ex2(masked(part[cc + 1], q4 * 32 + cc + 1) - m_run) : 0.0f;
-                            l_run += p0 + p1;
+                            const int cc = (q8 & 3) * 8 + 2 * e2;
+                            const float p0 = __uint_as_float(q8 < 4 ? pa[cc] : pb[cc]);
+                            const float p1 = __uint_as_float(q8 < 4 ? pa[cc + 1] : pb[cc + 1]);
+                            la[e2] += p0 + p1;
                             __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
                             w[e2] = *reinterpret_cast<uint32_t*>(&pk);
                         }
-                        *reinterpret_cast<uint4*>(pt + sw128_offset(tw, q4 * 4 + q8)) = make_uint4(w[0], w[1], w[2], w[3]);
+                        *reinterpret_cast<uint4*>(pt + sw128_offset(tw, h2 * 8 + q8)) = make_uint4(w[0], w[1], w[2], w[3]);
                     }
                 }
+                l_run += (la[0] + la[1]) + (la[2] + la[3]);
             }
             // the last tile's V rows past the key range are zeroed before the PV product
             // (they may hold stale or foreign data; P is 0 there but 0 * NaN is NaN)

@@ -14,12 +14,17 @@
 // CTAs of a cluster (up to 16) and over their threads; every thread keeps its
 // slice of the current node's logits (and, after a rejection, draft probabilities)
 // in registers, loaded with coalesced 128-bit loads.  Reductions go warp shuffles
-// (fp32) -> one warp per CTA (fp64) -> DSMEM across the cluster (fp64); every CTA
-// combines the cluster partials in the same order, so all CTAs hold bit-identical
-// scalars and take identical decisions without a second exchange.  The rows of the
-// current node's children and its draft row are prefetched into L2 while the
-// current row is reduced.  The p(x)/q(x) ratio is evaluated in fp64 from the
-// reduced scalars.
+// (fp32) -> one warp per CTA -> DSMEM across the cluster; every CTA combines the
+// cluster partials in the same order, so all CTAs hold bit-identical scalars and
+// take identical decisions without a second exchange.  The first child's logits
+// row and the node's draft row are prefetched into L2 while the current row is
+// reduced.
+//
+// Precision without fp64: GB300's fp64 rate is a small fraction of fp32, so sums
+// across threads, warps and CTAs are carried as float-float pairs (error-free
+// two-sum/two-product transformations, about 44 significant bits), and the
+// acceptance ratio p(x)/q(x) is formed in float-float from a compensated exponent
+// argument; its error is dominated by expf's (<= 2 ulp), a few 1e-7 relative.
 #include <cooperative_groups.h>
 
 #include "common.cuh"
@@ -29,14 +34,49 @@ namespace cg = cooperative_groups;
 
 namespace tsv {
 
-struct __align__(16) RedSlot {
-    double a;
-    double b;
-    int i;
-    int flag;
-};
-
 constexpr int kMaxRejections = kMaxNodes;  // at most one per tried child
+
+// ----------------------------------------------------------------------------- float-float
+
+struct ff {
+    float hi, lo;
+};
+__device__ __forceinline__ ff ff_make(float a) { return ff{a, 0.0f}; }
+// a + b exactly as hi + lo (Knuth's two-sum)
+__device__ __forceinline__ ff two_sum(float a, float b) {
+    const float s = a + b;
+    const float bb = s - a;
+    const float e = (a - (s - bb)) + (b - bb);
+    return ff{s, e};
+}
+// the same when |a| >= |b| (Dekker's fast two-sum)
+__device__ __forceinline__ ff quick_two_sum(float a, float b) {
+    const float s = a + b;
+    return ff{s, b - (s - a)};
+}
+__device__ __forceinline__ ff ff_add(ff a, ff b) {
+    const ff s = two_sum(a.hi, b.hi);
+    return quick_two_sum(s.hi, s.lo + (a.lo + b.lo));
+}
+__device__ __forceinline__ ff ff_sub(ff a, ff b) { return ff_add(a, ff{-b.hi, -b.lo}); }
+__device__ __forceinline__ ff ff_mul_f(ff a, float b) {
+    const float p = a.hi * b;
+    float e = fmaf(a.hi, b, -p);
+    e = fmaf(a.lo, b, e);
+    return quick_two_sum(p, e);
+}
+__device__ __forceinline__ ff ff_div(ff a, ff b) {
+    const float q1 = a.hi / b.hi;
+    const ff r = ff_sub(a, ff_mul_f(b, q1));
+    const float q2 = r.hi / b.hi;
+    return quick_two_sum(q1, q2);
+}
+__device__ __forceinline__ float ff_float(ff a) { return a.hi + a.lo; }
+__device__ __forceinline__ bool ff_pos(ff a) { return a.hi > 0.0f || (a.hi == 0.0f && a.lo > 0.0f); }
+__device__ __forceinline__ bool ff_lt(ff a, ff b) { return ff_pos(ff_sub(b, a)); }
+__device__ __forceinline__ ff ff_max0(ff a) { return ff_pos(a) ? a : ff_make(0.0f); }
+
+// ----------------------------------------------------------------------------- warp helpers
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -48,14 +88,12 @@ __device__ __forceinline__ float warp_sum(float v) {
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
-__device__ __forceinline__ double warp_sum_d(double v) {
+__device__ __forceinline__ ff warp_sum_ff(ff v) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
-__device__ __forceinline__ double warp_max_d(double v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmax(v, __shfl_xor_sync(0xffffffffu, v, o));
+    for (int o = 16; o > 0; o >>= 1) {
+        ff w{__shfl_xor_sync(0xffffffffu, v.hi, o), __shfl_xor_sync(0xffffffffu, v.lo, o)};
+        v = ff_add(v, w);
+    }
     return v;
 }
 __device__ __forceinline__ int warp_or(int v) {
@@ -67,8 +105,8 @@ __device__ __forceinline__ int warp_or(int v) {
 __device__ __forceinline__ void warp_argmax(float& v, int& i) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-        float v2 = __shfl_xor_sync(0xffffffffu, v, o);
-        int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+        const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+        const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
         if (v2 > v || (v2 == v && i2 < i)) {
             v = v2;
             i = i2;
@@ -83,9 +121,7 @@ __device__ __forceinline__ bool is_rejected(int v, int j, const int* xr) {
     return false;
 }
 
-__device__ __forceinline__ void prefetch_l2(const void* p) {
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
-}
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
 template <int VEC, bool ALIGNED>
 __device__ __forceinline__ void load_slice(const float* row, int v0, int v1, float (&x)[VEC][4], float fill) {
@@ -94,7 +130,7 @@ __device__ __forceinline__ void load_slice(const float* row, int v0, int v1, flo
         const int base = v0 + (k * (int)blockDim.x + (int)threadIdx.x) * 4;
         if (ALIGNED) {
             if (base < v1) {
-                float4 t = __ldg(reinterpret_cast<const float4*>(row + base));
+                const float4 t = __ldg(reinterpret_cast<const float4*>(row + base));
                 x[k][0] = t.x;
                 x[k][1] = t.y;
                 x[k][2] = t.z;
@@ -114,9 +150,72 @@ __device__ __forceinline__ void prefetch_slice(const float* row, int v0, int v1)
 #pragma unroll
     for (int k = 0; k < VEC; ++k) {
         const int base = v0 + (k * (int)blockDim.x + (int)threadIdx.x) * 4;
-        // one prefetch per 128-byte line: every 8th thread of a coalesced float4 run
+        // one prefetch per 128-byte line: the thread whose float4 starts the line
         if (base < v1 && ((reinterpret_cast<uintptr_t>(row + base) & 127) < 16)) prefetch_l2(row + base);
     }
+}
+
+// One CTA's contribution to a cluster reduction.
+struct __align__(16) RedSlot {
+    float a;   // max / argmax value
+    float hi;  // float-float sum (or second sum's hi in kind 1)
+    float lo;
+    int i;     // argmax index, or second sum's hi bits
+    int flag;  // OR-ed error flag
+    float hi2, lo2;
+    int pad;
+};
+
+enum { kRedStats = 0, kRedSums = 1, kRedArgmax = 2 };
+
+// Cluster all-reduce: every CTA publishes `mine` in its own slot[parity], the
+// cluster synchronises, and warp 0 of every CTA combines all slots in rank order
+// (so every CTA obtains bit-identical results).  Stats: (max a, sum hi+lo of
+// exp((x - a)/T)) with per-slot rescaling; sums: two float-float sums; argmax:
+// (a, i).  Must be called by every thread of every CTA; the result is in *res
+// after the closing __syncthreads.  Slots alternate by parity, so the write of the
+// next reduction cannot overtake a slow CTA still reading this one.
+__device__ __forceinline__ void cluster_allreduce(cg::cluster_group& cluster, RedSlot* slots, int parity,
+                                                  const RedSlot& mine, int kind, float T, RedSlot* res) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int cs = (int)cluster.num_blocks();
+    if (tid == 0) slots[parity] = mine;
+    cluster.sync();
+    if (tid < 32) {
+        RedSlot r{};
+        r.a = -INFINITY;
+        r.i = 0x7fffffff;
+        if (lane < cs) r = *cluster.map_shared_rank(&slots[parity], lane);
+        const int flag = warp_or(lane < cs ? r.flag : 0);
+        RedSlot o{};
+        o.flag = flag;
+        if (kind == kRedStats) {
+            const float m = warp_max(lane < cs ? r.a : -INFINITY);
+            ff c = ff_make(0.0f);
+            if (lane < cs && (r.hi > 0.0f)) c = ff_mul_f(ff{r.hi, r.lo}, expf((r.a - m) / T));
+            c = warp_sum_ff(c);
+            o.a = m;
+            o.hi = c.hi;
+            o.lo = c.lo;
+        } else if (kind == kRedSums) {
+            ff c1 = lane < cs ? ff{r.hi, r.lo} : ff_make(0.0f);
+            ff c2 = lane < cs ? ff{r.hi2, r.lo2} : ff_make(0.0f);
+            c1 = warp_sum_ff(c1);
+            c2 = warp_sum_ff(c2);
+            o.hi = c1.hi;
+            o.lo = c1.lo;
+            o.hi2 = c2.hi;
+            o.lo2 = c2.lo;
+        } else {
+            float v = lane < cs ? r.a : -INFINITY;
+            int i = lane < cs ? r.i : 0x7fffffff;
+            warp_argmax(v, i);
+            o.a = v;
+            o.i = i;
+        }
+        if (lane == 0) *res = o;
+    }
+    __syncthreads();
 }
 
 template <int VEC, bool ALIGNED>
@@ -129,111 +228,86 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
     const int N = a.N, V = a.V;
     const int v0 = min(V, rank * a.v_per_cta), v1 = min(V, v0 + a.v_per_cta);
     const bool greedy = (a.T == 0.0f);
-    const double Td = (double)a.T;
+    const float T = a.T;
 
     __shared__ int s_par[kMaxNodes], s_tok[kMaxNodes], s_path[kMaxNodes];
     __shared__ int s_kids[kMaxNodes];
     __shared__ float s_lx[kMaxNodes], s_qx[kMaxNodes], s_ux[kMaxNodes];
     __shared__ RedSlot s_red[2];
+    __shared__ RedSlot s_cta;  // this CTA's partial
+    __shared__ RedSlot s_all;  // cluster result
     __shared__ float s_wf[32], s_wg[32];
     __shared__ int s_wi[32], s_wb[32];
-    __shared__ double s_res[4];
-    __shared__ int s_ires[4];
-    __shared__ int s_flag;
+    __shared__ int s_nk, s_flag, s_accept, s_err2;
+    __shared__ float s_invz;
     // rejection history at the current node
-    __shared__ int s_xrej[kMaxRejections];        // rejected tokens x_1.. at the current node
+    __shared__ int s_xrej[kMaxRejections];        // rejected tokens x_1..x_j
     __shared__ float s_qrej[kMaxRejections];      // their raw draft probabilities
-    __shared__ double s_zr[kMaxRejections + 1];   // residual sums Zr_j (level j >= 1)
-    __shared__ double s_sq[kMaxRejections + 1];   // S_j = sum of q over tokens not in {x_1..x_j}
+    __shared__ ff s_zr[kMaxRejections + 1];       // residual sums Zr_j (level j >= 1)
+    __shared__ ff s_sq[kMaxRejections + 1];       // S_j = sum of q over tokens not in {x_1..x_j}
     __shared__ float s_inv_zr[kMaxRejections + 1], s_inv_sq[kMaxRejections + 1];
     __shared__ int s_zr_ok[kMaxRejections + 1];
+    __shared__ float s_seg[8 * 16];  // bonus: [k][warp] segment sums
+    __shared__ ff s_segcum[8 * 16];  // bonus: inclusive prefix over (k, warp)
+    __shared__ ff s_target;
+    __shared__ int s_claim, s_segsel;
 
     int parity = 0;
-    // Cluster all-reduce of one (a, b, i, flag) partial per CTA.  kind 0: (max, rescaled
-    // sum) softmax statistics; kind 1: (sum, sum); kind 2: argmax (value in a, index in i).
-    // Called by all threads of all CTAs.  Result in s_res[0..1], s_ires[0], s_ires[1].
-    auto cluster_combine = [&](double pa, double pb, int pi, int pflag, int kind) {
-        if (tid == 0) s_red[parity] = RedSlot{pa, pb, pi, pflag};
-        cluster.sync();
-        if (warp == 0) {
-            double ra = (kind == 1) ? 0.0 : -INFINITY, rb = 0.0;
-            int ri = 0x7fffffff, rf = 0;
-            if (lane < cs) {
-                const RedSlot* rs = cluster.map_shared_rank(&s_red[parity], lane);
-                ra = rs->a;
-                rb = rs->b;
-                ri = rs->i;
-                rf = rs->flag;
-            }
-            rf = warp_or(rf);
-            if (kind == 0) {
-                double m = warp_max_d(ra);
-                double s = (lane < cs && rb > 0.0) ? rb * exp((ra - m) / Td) : 0.0;
-                s = warp_sum_d(s);
-                ra = m;
-                rb = s;
-            } else if (kind == 1) {
-                ra = warp_sum_d(ra);
-                rb = warp_sum_d(rb);
-            } else {
-                float fv = (float)ra;
-                warp_argmax(fv, ri);
-                ra = fv;
-            }
-            if (lane == 0) {
-                s_res[0] = ra;
-                s_res[1] = rb;
-                s_ires[0] = ri;
-                s_ires[1] = rf;
-            }
-        }
-        parity ^= 1;
-        __syncthreads();
-    };
 
     // ---- tree and tokens
     for (int i = tid; i < N; i += blockDim.x) {
         s_par[i] = a.parent[(long long)b * N + i];
         s_tok[i] = a.tokens[(long long)b * N + i];
     }
-    bool tree_ok = block_tree_ok(a.parent + (long long)b * N, N, &s_flag);
+    const bool tree_ok = block_tree_ok(a.parent + (long long)b * N, N, &s_flag);
 
     int err = tree_ok ? 0 : TSV_DERR_PARENT;
     int node = 0, plen = 1;
     if (tid == 0) s_path[0] = 0;
     float lv[VEC][4], qv[VEC][4];
+#pragma unroll
+    for (int k = 0; k < VEC; ++k)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) qv[k][e] = 0.0f;
     int nrej = 0;
-    bool q_loaded = false;
-    double M = 0.0, Z = 1.0, Qsum = 0.0;
+    float M = 0.0f;
+    ff Z = ff_make(1.0f), Qsum = ff_make(0.0f);
     int amax = 0;
 
     while (!err) {
         const float* lrow = a.logits + ((long long)b * N + node) * V;
         const float* qrow = greedy ? nullptr : a.probs + ((long long)b * N + node) * V;
-        // children of `node`, in index order (identical in every thread)
-        if (tid == 0) {
+        // children of `node`, in index order (warp 0, by ballot)
+        if (warp == 0) {
             int nk = 0;
-            for (int c = node + 1; c < N; ++c)
-                if (s_par[c] == node) s_kids[nk++] = c;
-            s_ires[2] = nk;
+            for (int base = node + 1; base < N; base += 32) {
+                const int c = base + lane;
+                const bool is_kid = c < N && s_par[c] == node;
+                const unsigned m = __ballot_sync(0xffffffffu, is_kid);
+                if (is_kid) s_kids[nk + __popc(m & ((1u << lane) - 1u))] = c;
+                nk += __popc(m);
+            }
+            if (lane == 0) s_nk = nk;
         }
         __syncthreads();
-        const int nk = s_ires[2];
-        // scalar fetches for the children's tests, issued before the row pass
-        for (int t = tid; t < nk; t += blockDim.x) {
-            const int x = s_tok[s_kids[t]];
-            if (x >= 0 && x < V) {
-                s_lx[t] = __ldg(lrow + x);
-                if (!greedy) {
-                    s_qx[t] = __ldg(qrow + x);
-                    s_ux[t] = __ldg(a.u_accept + (long long)b * N + s_kids[t]);
+        const int nk = s_nk;
+        // the last warp fetches the scalars the children's tests need; the rest of the
+        // block starts on the row
+        if (warp == nwarps - 1) {
+            for (int t = lane; t < nk; t += 32) {
+                const int x = s_tok[s_kids[t]];
+                if (x >= 0 && x < V) {
+                    s_lx[t] = __ldg(lrow + x);
+                    if (!greedy) {
+                        s_qx[t] = __ldg(qrow + x);
+                        s_ux[t] = __ldg(a.u_accept + (long long)b * N + s_kids[t]);
+                    }
                 }
             }
         }
         load_slice<VEC, ALIGNED>(lrow, v0, v1, lv, -INFINITY);
-        // prefetch the children's logits rows and this node's draft row into L2
-        for (int t = 0; t < nk && t < 4; ++t)
-            prefetch_slice<VEC>(a.logits + ((long long)b * N + s_kids[t]) * V, v0, v1);
+        // likely next rows into L2: the first child's logits row and this node's draft row
+        if (nk > 0) prefetch_slice<VEC>(a.logits + ((long long)b * N + s_kids[0]) * V, v0, v1);
         if (!greedy && nk > 0) prefetch_slice<VEC>(qrow, v0, v1);
 
         int bad = 0;
@@ -269,70 +343,75 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
             if (warp == 0) {
                 float v = lane < nwarps ? s_wf[lane] : -INFINITY;
                 int i = lane < nwarps ? s_wi[lane] : 0x7fffffff;
-                int f = lane < nwarps ? s_wb[lane] : 0;
+                const int f = warp_or(lane < nwarps ? s_wb[lane] : 0);
                 warp_argmax(v, i);
-                f = warp_or(f);
                 if (lane == 0) {
-                    s_res[2] = v;
-                    s_ires[3] = i;
-                    s_flag = f;
+                    RedSlot m{};
+                    m.a = v;
+                    m.i = i;
+                    m.flag = f;
+                    s_cta = m;
                 }
             }
             __syncthreads();
-            cluster_combine(s_res[2], 0.0, s_ires[3], s_flag, 2);
-            amax = s_ires[0];
+            cluster_allreduce(cluster, s_red, parity, s_cta, kRedArgmax, T, &s_all);
+            parity ^= 1;
+            amax = s_all.i;
         } else {
+            // per warp: max m_w and sum of exp((l - m_w)/T) in fp32
             float m = -INFINITY;
 #pragma unroll
             for (int k = 0; k < VEC; ++k)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) m = fmaxf(m, lv[k][e]);
             m = warp_max(m);
-            float s = 0.0f;
+            float sacc = 0.0f;
             if (m > -INFINITY) {
 #pragma unroll
                 for (int k = 0; k < VEC; ++k)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) s += expf((lv[k][e] - m) / a.T);
+                    for (int e = 0; e < 4; ++e) sacc += expf((lv[k][e] - m) / T);
             }
-            s = warp_sum(s);
+            sacc = warp_sum(sacc);
             bad = warp_or(bad);
             if (lane == 0) {
                 s_wf[warp] = m;
-                s_wg[warp] = s;
-                s_wi[warp] = bad;
+                s_wg[warp] = sacc;
+                s_wb[warp] = bad;
             }
             __syncthreads();
             if (warp == 0) {
-                double wm = lane < nwarps ? (double)s_wf[lane] : -INFINITY;
-                double ws = lane < nwarps ? (double)s_wg[lane] : 0.0;
-                int f = lane < nwarps ? s_wi[lane] : 0;
-                double cm = warp_max_d(wm);
-                double cs_ = (ws > 0.0) ? ws * exp((wm - cm) / Td) : 0.0;
-                cs_ = warp_sum_d(cs_);
-                f = warp_or(f);
+                const float wm = lane < nwarps ? s_wf[lane] : -INFINITY;
+                const float ws = lane < nwarps ? s_wg[lane] : 0.0f;
+                const int f = warp_or(lane < nwarps ? s_wb[lane] : 0);
+                const float cm = warp_max(wm);
+                ff c = ws > 0.0f ? ff_mul_f(ff_make(ws), expf((wm - cm) / T)) : ff_make(0.0f);
+                c = warp_sum_ff(c);
                 if (lane == 0) {
-                    s_res[2] = cm;
-                    s_res[3] = cs_;
-                    s_flag = f;
+                    RedSlot r{};
+                    r.a = cm;
+                    r.hi = c.hi;
+                    r.lo = c.lo;
+                    r.flag = f;
+                    s_cta = r;
                 }
             }
             __syncthreads();
-            cluster_combine(s_res[2], s_res[3], 0, s_flag, 0);
-            M = s_res[0];
-            Z = s_res[1];
+            cluster_allreduce(cluster, s_red, parity, s_cta, kRedStats, T, &s_all);
+            parity ^= 1;
+            M = s_all.a;
+            Z = ff{s_all.hi, s_all.lo};
+            if (tid == 0) s_invz = ff_float(ff_div(ff_make(1.0f), Z));
         }
-        if (s_ires[1]) {
+        if (s_all.flag) {
             err = TSV_DERR_NONFINITE;
             break;
         }
 
         // ---- children, in index order
         nrej = 0;
-        q_loaded = false;
+        bool q_loaded = false;
         int next = -1;
-        const float invZ = (float)(1.0 / Z);
-        const float Mf = (float)M;  // M is the max of float logits: exact
         for (int t = 0; t < nk; ++t) {
             const int c = s_kids[t];
             const int x = s_tok[c];
@@ -347,33 +426,37 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                 }
                 continue;
             }
-            // q(x) at the current level and the fp64 ratio (thread 0; broadcast)
+            // p(x)/q(x) at the current level, in float-float (thread 0; broadcast)
             if (tid == 0) {
                 const float qraw = s_qx[t];
-                int e2 = 0;
-                double ratio = 0.0;
+                int e2 = 0, acc = 0;
                 if (!isfinite(qraw)) {
                     e2 = TSV_DERR_NONFINITE;
                 } else {
-                    double px = exp(((double)s_lx[t] - M) / Td) / Z;
-                    double qx = (double)qraw;  // level 0: the raw draft probability
+                    // p_0(x) = exp((l_x - M) / T) / Z with a compensated exponent argument
+                    const ff arg = ff_div(two_sum(s_lx[t], -M), ff_make(T));
+                    const float ex = expf(arg.hi);
+                    ff px = ff_div(quick_two_sum(ex, ex * arg.lo), Z);
+                    ff qx = ff_make(qraw);  // level 0: the raw draft probability
                     bool x_rejected = false;
                     for (int j = 1; j <= nrej; ++j) {
                         // level j-1 -> j: residual on p, x_j removed from q
-                        if (s_zr_ok[j]) px = fmax(0.0, px - qx) / s_zr[j];
+                        if (s_zr_ok[j]) px = ff_div(ff_max0(ff_sub(px, qx)), s_zr[j]);
                         if (s_xrej[j - 1] == x) x_rejected = true;
-                        qx = (x_rejected || !(s_sq[j] > 0.0)) ? 0.0 : (double)qraw / s_sq[j];
+                        qx = (x_rejected || !ff_pos(s_sq[j])) ? ff_make(0.0f) : ff_div(ff_make(qraw), s_sq[j]);
                     }
-                    if (qx > 0.0)
-                        ratio = px / qx;
+                    // u < p/q, i.e. u * q < p (q > 0); q == 0 accepts iff p > 0
+                    const float u = s_ux[t];
+                    if (ff_pos(qx))
+                        acc = ff_lt(ff_mul_f(qx, u), px) ? 1 : 0;
                     else
-                        ratio = (px > 0.0) ? INFINITY : 0.0;
+                        acc = ff_pos(px) ? 1 : 0;
                 }
-                s_ires[2] = e2;
-                s_ires[3] = (e2 == 0 && (double)s_ux[t] < ratio) ? 1 : 0;
+                s_err2 = e2;
+                s_accept = acc;
             }
             __syncthreads();
-            const int e2 = s_ires[2], accept = s_ires[3];
+            const int e2 = s_err2, accept = s_accept;
             __syncthreads();
             if (e2) {
                 err = e2;
@@ -384,9 +467,9 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                 break;
             }
             // rejected: residual sum at the next level (and, the first time, sum q)
+            int qb = 0;
             if (!q_loaded) {
                 load_slice<VEC, ALIGNED>(qrow, v0, v1, qv, 0.0f);
-                int qb = 0;
 #pragma unroll
                 for (int k = 0; k < VEC; ++k)
 #pragma unroll
@@ -394,75 +477,75 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                         const int v = v0 + (k * (int)blockDim.x + tid) * 4 + e;
                         if (v < v1 && !isfinite(qv[k][e])) qb = 1;
                     }
-                qb = warp_or(qb);
-                if (lane == 0) s_wi[warp] = qb;
-            } else if (lane == 0) {
-                s_wi[warp] = 0;
             }
+            const float invZ = s_invz;
             float zr = 0.0f, qs = 0.0f;
 #pragma unroll
             for (int k = 0; k < VEC; ++k)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int v = v0 + (k * (int)blockDim.x + tid) * 4 + e;
-                    float p = expf((lv[k][e] - Mf) / a.T) * invZ;
-                    float q = qv[k][e];
+                    float p = expf((lv[k][e] - M) / T) * invZ;
+                    const float q = qv[k][e];
                     for (int j = 1; j <= nrej; ++j) {
                         const float qprev =
                             (j == 1) ? q : (is_rejected(v, j - 1, s_xrej) ? 0.0f : q * s_inv_sq[j - 1]);
                         if (s_zr_ok[j]) p = fmaxf(0.0f, p - qprev) * s_inv_zr[j];
                     }
-                    const float qcur =
-                        (nrej == 0) ? q : (is_rejected(v, nrej, s_xrej) ? 0.0f : q * s_inv_sq[nrej]);
+                    const float qcur = (nrej == 0) ? q : (is_rejected(v, nrej, s_xrej) ? 0.0f : q * s_inv_sq[nrej]);
                     zr += fmaxf(0.0f, p - qcur);
-                    if (!q_loaded) qs += q;
+                    qs += q;
                 }
             zr = warp_sum(zr);
             qs = warp_sum(qs);
+            qb = warp_or(qb);
             if (lane == 0) {
                 s_wf[warp] = zr;
                 s_wg[warp] = qs;
+                s_wb[warp] = qb;
             }
             __syncthreads();
             if (warp == 0) {
-                double z1 = lane < nwarps ? (double)s_wf[lane] : 0.0;
-                double z2 = lane < nwarps ? (double)s_wg[lane] : 0.0;
-                int f = lane < nwarps ? s_wi[lane] : 0;
-                z1 = warp_sum_d(z1);
-                z2 = warp_sum_d(z2);
-                f = warp_or(f);
+                const ff z1 = warp_sum_ff(ff_make(lane < nwarps ? s_wf[lane] : 0.0f));
+                const ff z2 = warp_sum_ff(ff_make(lane < nwarps ? s_wg[lane] : 0.0f));
+                const int f = warp_or(lane < nwarps ? s_wb[lane] : 0);
                 if (lane == 0) {
-                    s_res[2] = z1;
-                    s_res[3] = z2;
-                    s_flag = f;
+                    RedSlot r{};
+                    r.hi = z1.hi;
+                    r.lo = z1.lo;
+                    r.hi2 = z2.hi;
+                    r.lo2 = z2.lo;
+                    r.flag = f;
+                    s_cta = r;
                 }
             }
             __syncthreads();
-            cluster_combine(s_res[2], s_res[3], 0, s_flag, 1);
-            if (s_ires[1]) {
+            cluster_allreduce(cluster, s_red, parity, s_cta, kRedSums, T, &s_all);
+            parity ^= 1;
+            if (s_all.flag) {
                 err = TSV_DERR_NONFINITE;
                 break;
             }
-            if (!q_loaded) Qsum = s_res[1];
+            if (!q_loaded) Qsum = ff{s_all.hi2, s_all.lo2};
             q_loaded = true;
-            // record level nrej+1 (every thread holds the same values)
-            const double zr_new = s_res[0];
+            // record level nrej + 1
+            const ff zr_new{s_all.hi, s_all.lo};
             __syncthreads();
             if (tid == 0) {
                 const int j = nrej + 1;
                 s_xrej[j - 1] = x;
                 s_qrej[j - 1] = s_qx[t];
                 s_zr[j] = zr_new;
-                s_zr_ok[j] = zr_new > 0.0;
-                s_inv_zr[j] = zr_new > 0.0 ? (float)(1.0 / zr_new) : 1.0f;
-                double sq = Qsum;
+                s_zr_ok[j] = ff_pos(zr_new);
+                s_inv_zr[j] = ff_pos(zr_new) ? ff_float(ff_div(ff_make(1.0f), zr_new)) : 1.0f;
+                ff sq = Qsum;
                 for (int i2 = 0; i2 < j; ++i2) {  // subtract each distinct rejected token once
                     bool dup = false;
                     for (int i3 = 0; i3 < i2; ++i3) dup |= (s_xrej[i3] == s_xrej[i2]);
-                    if (!dup) sq -= (double)s_qrej[i2];
+                    if (!dup) sq = ff_sub(sq, ff_make(s_qrej[i2]));
                 }
                 s_sq[j] = sq;
-                s_inv_sq[j] = sq > 0.0 ? (float)(1.0 / sq) : 0.0f;
+                s_inv_sq[j] = ff_pos(sq) ? ff_float(ff_div(ff_make(1.0f), sq)) : 0.0f;
             }
             __syncthreads();
             ++nrej;
@@ -510,17 +593,16 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
         return;
     }
 
-    // ---- bonus: inverse CDF of the current p over token order
-    // per-thread 4-element sums for every vector step k; token order within a CTA is
-    // (k, warp, lane, element)
-    const float invZ = (float)(1.0 / Z);
-    float (&pk)[VEC][4] = lv;  // the logits slice is not needed after this pass
+    // ---- bonus: inverse CDF of the current p in token order.  Token order within a
+    // CTA is (vector step k, warp, lane, element); prefix sums are float-float.
+    const float invZ = s_invz;
+    float(&pk)[VEC][4] = lv;  // the logits slice is not needed after this pass
 #pragma unroll
     for (int k = 0; k < VEC; ++k)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int v = v0 + (k * (int)blockDim.x + tid) * 4 + e;
-            float p = expf((lv[k][e] - (float)M) / a.T) * invZ;
+            float p = expf((lv[k][e] - M) / T) * invZ;
             const float q = qv[k][e];
             for (int j = 1; j <= nrej; ++j) {
                 const float qprev = (j == 1) ? q : (is_rejected(v, j - 1, s_xrej) ? 0.0f : q * s_inv_sq[j - 1]);
@@ -528,99 +610,99 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
             }
             pk[k][e] = (v < v1) ? p : 0.0f;
         }
-    __shared__ float s_seg[8 * 16];     // [k][warp] segment sums
-    __shared__ double s_segcum[8 * 16];  // inclusive prefix over (k, warp)
 #pragma unroll
     for (int k = 0; k < VEC; ++k) {
-        float ts = pk[k][0] + pk[k][1] + pk[k][2] + pk[k][3];
-        ts = warp_sum(ts);
+        const float ts = warp_sum(pk[k][0] + pk[k][1] + pk[k][2] + pk[k][3]);
         if (lane == 0) s_seg[k * nwarps + warp] = ts;
     }
     __syncthreads();
     const int nseg = VEC * nwarps;
     if (warp == 0) {
-        // each lane owns a run of consecutive segments; fp64 prefix.  Each level's
-        // exclusive base is the previous level's inclusive value itself (never a
-        // difference), so the intervals tile [0, total) exactly.
+        // each lane owns a run of consecutive segments.  Each level's exclusive base is
+        // the previous level's inclusive value itself (never a difference), so the
+        // intervals tile [0, total) exactly.
         const int per = (nseg + 31) / 32;
-        double run = 0.0;
-        for (int s = lane * per; s < min(nseg, lane * per + per); ++s) run += (double)s_seg[s];
-        double incl = run;
+        ff run = ff_make(0.0f);
+        for (int s2 = lane * per; s2 < min(nseg, lane * per + per); ++s2) run = ff_add(run, ff_make(s_seg[s2]));
+        ff incl = run;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            double y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
+            const ff y{__shfl_up_sync(0xffffffffu, incl.hi, o), __shfl_up_sync(0xffffffffu, incl.lo, o)};
+            if (lane >= o) incl = ff_add(incl, y);
         }
-        double base = __shfl_up_sync(0xffffffffu, incl, 1);
-        if (lane == 0) base = 0.0;
-        for (int s = lane * per; s < min(nseg, lane * per + per); ++s) {
-            base += (double)s_seg[s];
-            s_segcum[s] = base;
+        ff base{__shfl_up_sync(0xffffffffu, incl.hi, 1), __shfl_up_sync(0xffffffffu, incl.lo, 1)};
+        if (lane == 0) base = ff_make(0.0f);
+        for (int s2 = lane * per; s2 < min(nseg, lane * per + per); ++s2) {
+            base = ff_add(base, ff_make(s_seg[s2]));
+            s_segcum[s2] = base;
         }
     }
     __syncthreads();
-    if (tid == 0) s_res[2] = s_segcum[nseg - 1];  // CTA total
-    __syncthreads();
-    // cluster exclusive prefix of CTA totals
-    if (tid == 0) s_red[parity] = RedSlot{s_res[2], 0.0, 0, 0};
+    if (tid == 0) {
+        RedSlot r{};
+        r.hi = s_segcum[nseg - 1].hi;  // CTA total
+        r.lo = s_segcum[nseg - 1].lo;
+        s_red[parity] = r;
+    }
     cluster.sync();
     if (warp == 0) {
-        double tot = 0.0;
-        if (lane < cs) tot = cluster.map_shared_rank(&s_red[parity], lane)->a;
-        double incl = tot;
+        ff tot = ff_make(0.0f);
+        if (lane < cs) {
+            const RedSlot* rs = cluster.map_shared_rank(&s_red[parity], lane);
+            tot = ff{rs->hi, rs->lo};
+        }
+        ff incl = tot;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            double y = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += y;
+            const ff y{__shfl_up_sync(0xffffffffu, incl.hi, o), __shfl_up_sync(0xffffffffu, incl.lo, o)};
+            if (lane >= o) incl = ff_add(incl, y);
         }
-        double excl = __shfl_up_sync(0xffffffffu, incl, 1);
-        if (lane == 0) excl = 0.0;
-        const double grand = __shfl_sync(0xffffffffu, incl, cs - 1);
-        const double mine_incl = __shfl_sync(0xffffffffu, incl, rank);
-        const double mine_excl = __shfl_sync(0xffffffffu, excl, rank);
+        ff excl{__shfl_up_sync(0xffffffffu, incl.hi, 1), __shfl_up_sync(0xffffffffu, incl.lo, 1)};
+        if (lane == 0) excl = ff_make(0.0f);
+        const ff grand{__shfl_sync(0xffffffffu, incl.hi, cs - 1), __shfl_sync(0xffffffffu, incl.lo, cs - 1)};
+        const ff mine_incl{__shfl_sync(0xffffffffu, incl.hi, rank), __shfl_sync(0xffffffffu, incl.lo, rank)};
+        const ff mine_excl{__shfl_sync(0xffffffffu, excl.hi, rank), __shfl_sync(0xffffffffu, excl.lo, rank)};
         if (lane == 0) {
-            const double target = (double)a.u_bonus[b] * grand;  // u in [0,1): target < grand
-            s_res[0] = mine_excl;
-            s_res[1] = target;
-            s_ires[0] = (target >= mine_excl && target < mine_incl) ? 1 : 0;
+            const ff target = ff_mul_f(grand, a.u_bonus[b]);  // u in [0,1): target < grand
+            s_target = ff_sub(target, mine_excl);
+            s_claim = (!ff_lt(target, mine_excl) && ff_lt(target, mine_incl)) ? 1 : 0;
         }
     }
     parity ^= 1;
     __syncthreads();
-    if (s_ires[0]) {
+    if (s_claim) {
         // this CTA holds the crossing: find the segment, then the lane, then the element
-        const double target = s_res[1] - s_res[0];
         if (tid == 0) {
+            const ff target = s_target;
             int seg = -1;
-            for (int s = 0; s < nseg; ++s)
-                if (target < s_segcum[s]) {
-                    seg = s;
+            for (int s2 = 0; s2 < nseg; ++s2)
+                if (ff_lt(target, s_segcum[s2])) {
+                    seg = s2;
                     break;
                 }
             if (seg < 0)  // only by rounding of the base subtraction: last segment with mass
-                for (int s = nseg - 1; s >= 0 && seg < 0; --s)
-                    if (s_seg[s] > 0.0f) seg = s;
-            s_ires[2] = seg;
-            s_res[3] = target - (seg > 0 ? s_segcum[seg - 1] : 0.0);
+                for (int s2 = nseg - 1; s2 >= 0 && seg < 0; --s2)
+                    if (s_seg[s2] > 0.0f) seg = s2;
+            s_segsel = seg;
+            s_target = seg > 0 ? ff_sub(target, s_segcum[seg - 1]) : target;
         }
         __syncthreads();
-        const int seg = s_ires[2];
+        const int seg = s_segsel;
         const int kseg = seg / nwarps, wseg = seg % nwarps;
         if (warp == wseg) {
-            const float tgt = (float)s_res[3];
-            float ts = 0.0f;
-            float pe[4];
+            const float tgt = ff_float(s_target);
+            float pe[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
             for (int k = 0; k < VEC; ++k)
                 if (k == kseg) {
 #pragma unroll
                     for (int e = 0; e < 4; ++e) pe[e] = pk[k][e];
                 }
-            ts = pe[0] + pe[1] + pe[2] + pe[3];
+            const float ts = pe[0] + pe[1] + pe[2] + pe[3];
             float incl = ts;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
-                float y = __shfl_up_sync(0xffffffffu, incl, o);
+                const float y = __shfl_up_sync(0xffffffffu, incl, o);
                 if (lane >= o) incl += y;
             }
             float excl = __shfl_up_sync(0xffffffffu, incl, 1);
@@ -630,13 +712,13 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
             // fp32 rounding can leave no lane past the target: take the last with mass
             const int l_sel = hit ? (__ffs(hit) - 1) : (31 - __clz(has));
             if (lane == l_sel) {
-                float c = excl;
+                float cum = excl;
                 int e_sel = -1, e_last = -1;
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     if (pe[e] > 0.0f) e_last = e;
-                    c += pe[e];
-                    if (e_sel < 0 && tgt < c && pe[e] > 0.0f) e_sel = e;
+                    cum += pe[e];
+                    if (e_sel < 0 && tgt < cum && pe[e] > 0.0f) e_sel = e;
                 }
                 if (e_sel < 0) e_sel = e_last;
                 const int tok = v0 + (kseg * (int)blockDim.x + tid) * 4 + e_sel;
