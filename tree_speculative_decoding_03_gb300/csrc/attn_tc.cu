@@ -332,8 +332,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the tile's j-th cache block and issues that block's boxes, so a tile's block
         // ids are fetched in one coalesced load instead of one dependent load each)
         const int nfills = 2 * ntiles;
+        // block id of this lane's cache block for fill f (K and V fills of a tile share ids);
+        // loaded before waiting for the fill's slot so the load latency is hidden
+        auto tile_block = [=](int f) -> int {
+            const int t0 = k_begin + (f >> 1) * kTileKeys;
+            const int nb = (min(t0 + kTileKeys, k_end) - t0 + bs - 1) >> a.bs_log2;
+            return lane < nb ? bt[(t0 >> a.bs_log2) + lane] : 0;
+        };
+        int blk_next = tile_block(0);
         for (int f = 0; f < nfills && !my_err; ++f) {
             const int slot = f % nslots, use = f / nslots;
+            const int blk = blk_next;
+            if (f + 1 < nfills) blk_next = ((f + 1) >> 1) == (f >> 1) ? blk : tile_block(f + 1);
             if (use > 0 && !__all_sync(0xffffffffu, mbar_wait(bar(Bars::kEmpty + slot), (use - 1) & 1, s_abort))) {
                 my_err = 1;
                 break;
@@ -345,11 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t dst = smem_u32(smem + lay.ring + slot * SLOT);
             if (lane == 0) mbar_expect_tx(bar(Bars::kFull + slot), static_cast<uint32_t>(nblk * bs * 128 * HALVES));
             __syncwarp();
-            for (int jb = lane; jb < nblk; jb += 32) {
-                const int blk = bt[(t0 >> a.bs_log2) + jb];
+            if (lane < nblk) {  // a 128-key tile spans at most 128 / 8 = 16 blocks
 #pragma unroll
                 for (int hh = 0; hh < HALVES; ++hh)
-                    tma_load_3d(dst + hh * kHalfBytes + jb * bs * 128, map, bar(Bars::kFull + slot), hh * 64, g,
+                    tma_load_3d(dst + hh * kHalfBytes + lane * bs * 128, map, bar(Bars::kFull + slot), hh * 64, g,
                                 blk * bs);
             }
         }
@@ -409,6 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     issue_PV(m, fV % nslots, j > 0);
                     mma_commit(bar(Bars::kO + m));
+                    if (m == nm - 1) mma_commit(bar(Bars::kEmpty + fV % nslots));  // V_j's last reader issued
                     if (j + 1 < ntiles) {
                         if (m == 0) {
                             ok = mbar_wait(bar(Bars::kFull + fK % nslots), (fK / nslots) & 1, s_abort);
@@ -420,7 +430,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 if (!ok) break;
-                mma_commit(bar(Bars::kEmpty + fV % nslots));
                 if (j + 1 < ntiles) mma_commit(bar(Bars::kEmpty + fK % nslots));
             }
             if (!ok) my_err = 1;
