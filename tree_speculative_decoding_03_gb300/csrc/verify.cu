@@ -27,6 +27,9 @@
 // argument; its error is dominated by expf's (<= 2 ulp), a few 1e-7 relative.
 #include <cooperative_groups.h>
 
+#include <map>
+#include <mutex>
+
 #include "common.cuh"
 #include "verify_args.cuh"
 
@@ -114,6 +117,14 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
     }
 }
 
+// x / T from a precomputed 1/T with one Newton correction (within an ulp of the
+// correctly rounded quotient; exact for T == 1) -- a full IEEE division per element
+// costs far more than the two FMAs
+__device__ __forceinline__ float div_t(float x, float T, float invT) {
+    const float q = x * invT;
+    return isfinite(q) ? fmaf(fmaf(-q, T, x), invT, q) : q;  // -inf (padding) stays -inf
+}
+
 // true iff v is one of the first j rejected tokens xr[0..j-1]
 __device__ __forceinline__ bool is_rejected(int v, int j, const int* xr) {
     for (int i = 0; i < j; ++i)
@@ -143,6 +154,42 @@ __device__ __forceinline__ void load_slice(const float* row, int v0, int v1, flo
             for (int e = 0; e < 4; ++e) x[k][e] = (base + e < v1) ? __ldg(row + base + e) : fill;
         }
     }
+}
+
+// this thread's 4 entries of vector step k (fill past v1)
+template <bool ALIGNED>
+__device__ __forceinline__ void load4(const float* row, int base, int v1, float (&x)[4], float fill) {
+    if (ALIGNED) {
+        if (base < v1) {
+            const float4 t = __ldg(reinterpret_cast<const float4*>(row + base));
+            x[0] = t.x;
+            x[1] = t.y;
+            x[2] = t.z;
+            x[3] = t.w;
+        } else {
+            x[0] = x[1] = x[2] = x[3] = fill;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) x[e] = (base + e < v1) ? __ldg(row + base + e) : fill;
+    }
+}
+
+// Bit (4k + e) set iff this thread's entry e of vector step k is one of the tokens
+// xr[0..n-1] (the rejected siblings at the current node): an O(n) scan per pass
+// instead of an O(n) membership test per entry.
+template <int VEC>
+__device__ __forceinline__ uint32_t owned_mask(const int* xr, int n, int v0, int v1) {
+    uint32_t m = 0u;
+    for (int i = 0; i < n; ++i) {
+        const int x = xr[i];
+        if (x < v0 || x >= v1) continue;
+        const int f = (x - v0) >> 2;
+        if (f % (int)blockDim.x != (int)threadIdx.x) continue;
+        const int k = f / (int)blockDim.x;
+        if (k < VEC) m |= 1u << (k * 4 + ((x - v0) & 3));
+    }
+    return m;
 }
 
 template <int VEC>
@@ -218,6 +265,32 @@ __device__ __forceinline__ void cluster_allreduce(cg::cluster_group& cluster, Re
     __syncthreads();
 }
 
+// Recomputes the normalised p of residual level `level` into the register slice from
+// the logits row and the recorded levels (the slow, per-entry chain; used only when a
+// residual sum is exactly zero).
+template <int VEC, bool ALIGNED>
+__device__ __forceinline__ void rebuild_level(float (&lv)[VEC][4], const float* lrow, const float* qrow, int v0, int v1,
+                                           int level, float M, float T, float invT, float invZ, const int* xrej,
+                                           const float* inv_sq, const float* inv_zr, const int* zr_ok) {
+    load_slice<VEC, ALIGNED>(lrow, v0, v1, lv, -INFINITY);
+#pragma unroll
+    for (int k = 0; k < VEC; ++k) {
+        const int base = v0 + (k * (int)blockDim.x + (int)threadIdx.x) * 4;
+        float qk[4];
+        load4<ALIGNED>(qrow, base, v1, qk, 0.0f);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int v = base + e;
+            float p = expf(div_t(lv[k][e] - M, T, invT)) * invZ;
+            for (int j = 1; j <= level; ++j) {
+                const float qprev = (j == 1) ? qk[e] : (is_rejected(v, j - 1, xrej) ? 0.0f : qk[e] * inv_sq[j - 1]);
+                if (zr_ok[j]) p = fmaxf(0.0f, p - qprev) * inv_zr[j];
+            }
+            lv[k][e] = (v < v1) ? p : 0.0f;
+        }
+    }
+}
+
 template <int VEC, bool ALIGNED>
 __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a) {
     cg::cluster_group cluster = cg::this_cluster();
@@ -229,6 +302,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
     const int v0 = min(V, rank * a.v_per_cta), v1 = min(V, v0 + a.v_per_cta);
     const bool greedy = (a.T == 0.0f);
     const float T = a.T;
+    const float invT = greedy ? 0.0f : 1.0f / a.T;
 
     __shared__ int s_par[kMaxNodes], s_tok[kMaxNodes], s_path[kMaxNodes];
     __shared__ int s_kids[kMaxNodes];
@@ -264,12 +338,15 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
     int err = tree_ok ? 0 : TSV_DERR_PARENT;
     int node = 0, plen = 1;
     if (tid == 0) s_path[0] = 0;
-    float lv[VEC][4], qv[VEC][4];
-#pragma unroll
-    for (int k = 0; k < VEC; ++k)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) qv[k][e] = 0.0f;
+    // the current node's logits slice stays in registers; its draft row is re-read (from
+    // L2, where it was prefetched) by the passes that need it, which keeps register
+    // pressure low enough for 32 entries per thread
+    float lv[VEC][4];
     int nrej = 0;
+    // After the first rejection at a node the register slice holds the unnormalised
+    // residual r instead of the logits; the current p is r * pscale.
+    bool lv_is_p = false;
+    float pscale = 0.0f;
     float M = 0.0f;
     ff Z = ff_make(1.0f), Qsum = ff_make(0.0f);
     int amax = 0;
@@ -367,10 +444,12 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
             m = warp_max(m);
             float sacc = 0.0f;
             if (m > -INFINITY) {
+                float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
                 for (int k = 0; k < VEC; ++k)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) sacc += expf((lv[k][e] - m) / T);
+                    for (int e = 0; e < 4; ++e) s4[e] += expf(div_t(lv[k][e] - m, T, invT));
+                sacc = (s4[0] + s4[1]) + (s4[2] + s4[3]);
             }
             sacc = warp_sum(sacc);
             bad = warp_or(bad);
@@ -410,6 +489,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
 
         // ---- children, in index order
         nrej = 0;
+        lv_is_p = false;
         bool q_loaded = false;
         int next = -1;
         for (int t = 0; t < nk; ++t) {
@@ -468,34 +548,36 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
             }
             // rejected: residual sum at the next level (and, the first time, sum q)
             int qb = 0;
-            if (!q_loaded) {
-                load_slice<VEC, ALIGNED>(qrow, v0, v1, qv, 0.0f);
+            const float invZ = s_invz;
+            const uint32_t excl = owned_mask<VEC>(s_xrej, nrej, v0, v1);  // tokens out of q at this level
+            const float inv_sq = nrej > 0 ? s_inv_sq[nrej] : 1.0f;
+            float zr = 0.0f, qs = 0.0f;
+            constexpr int QG = VEC < 4 ? VEC : 4;  // draft entries loaded per group of vector steps
 #pragma unroll
-                for (int k = 0; k < VEC; ++k)
+            for (int k0 = 0; k0 < VEC; k0 += QG) {
+                float qk[QG][4];
+#pragma unroll
+                for (int kk = 0; kk < QG; ++kk)
+                    load4<ALIGNED>(qrow, v0 + ((k0 + kk) * (int)blockDim.x + tid) * 4, v1, qk[kk], 0.0f);
+#pragma unroll
+                for (int kk = 0; kk < QG; ++kk) {
+                    const int k = k0 + kk;
+                    const int base = v0 + (k * (int)blockDim.x + tid) * 4;
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const int v = v0 + (k * (int)blockDim.x + tid) * 4 + e;
-                        if (v < v1 && !isfinite(qv[k][e])) qb = 1;
+                        const int v = base + e;
+                        const float q = qk[kk][e];
+                        if (v < v1 && !isfinite(q)) qb = 1;
+                        // p and q at the current level
+                        const float p = lv_is_p ? lv[k][e] * pscale : expf(div_t(lv[k][e] - M, T, invT)) * invZ;
+                        const float qc = (nrej == 0) ? q : (((excl >> (k * 4 + e)) & 1u) ? 0.0f : q * inv_sq);
+                        const float d = fmaxf(0.0f, p - qc);
+                        zr += d;
+                        qs += q;
+                        lv[k][e] = (v < v1) ? d : 0.0f;  // the residual replaces the slice
                     }
-            }
-            const float invZ = s_invz;
-            float zr = 0.0f, qs = 0.0f;
-#pragma unroll
-            for (int k = 0; k < VEC; ++k)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int v = v0 + (k * (int)blockDim.x + tid) * 4 + e;
-                    float p = expf((lv[k][e] - M) / T) * invZ;
-                    const float q = qv[k][e];
-                    for (int j = 1; j <= nrej; ++j) {
-                        const float qprev =
-                            (j == 1) ? q : (is_rejected(v, j - 1, s_xrej) ? 0.0f : q * s_inv_sq[j - 1]);
-                        if (s_zr_ok[j]) p = fmaxf(0.0f, p - qprev) * s_inv_zr[j];
-                    }
-                    const float qcur = (nrej == 0) ? q : (is_rejected(v, nrej, s_xrej) ? 0.0f : q * s_inv_sq[nrej]);
-                    zr += fmaxf(0.0f, p - qcur);
-                    qs += q;
                 }
+            }
             zr = warp_sum(zr);
             qs = warp_sum(qs);
             qb = warp_or(qb);
@@ -549,6 +631,17 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
             }
             __syncthreads();
             ++nrej;
+            if (s_zr_ok[nrej]) {
+                lv_is_p = true;
+                pscale = s_inv_zr[nrej];
+            } else {
+                // empty residual: p keeps its previous value, which the pass overwrote --
+                // rebuild it from the logits (unreachable in exact arithmetic)
+                rebuild_level<VEC, ALIGNED>(lv, lrow, qrow, v0, v1, nrej, M, T, invT, s_invz, s_xrej, s_inv_sq,
+                                            s_inv_zr, s_zr_ok);
+                lv_is_p = true;
+                pscale = 1.0f;
+            }
         }
         if (err || next < 0) break;
         if (tid == 0) s_path[plen] = next;
@@ -596,18 +689,13 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
     // ---- bonus: inverse CDF of the current p in token order.  Token order within a
     // CTA is (vector step k, warp, lane, element); prefix sums are float-float.
     const float invZ = s_invz;
-    float(&pk)[VEC][4] = lv;  // the logits slice is not needed after this pass
+    float(&pk)[VEC][4] = lv;  // the slice is not needed after this pass
 #pragma unroll
     for (int k = 0; k < VEC; ++k)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int v = v0 + (k * (int)blockDim.x + tid) * 4 + e;
-            float p = expf((lv[k][e] - M) / T) * invZ;
-            const float q = qv[k][e];
-            for (int j = 1; j <= nrej; ++j) {
-                const float qprev = (j == 1) ? q : (is_rejected(v, j - 1, s_xrej) ? 0.0f : q * s_inv_sq[j - 1]);
-                if (s_zr_ok[j]) p = fmaxf(0.0f, p - qprev) * s_inv_zr[j];
-            }
+            const float p = lv_is_p ? lv[k][e] * pscale : expf(div_t(lv[k][e] - M, T, invT)) * invZ;
             pk[k][e] = (v < v1) ? p : 0.0f;
         }
 #pragma unroll
@@ -735,53 +823,112 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
 namespace tsv {
 
 template <int VEC, bool ALIGNED>
-static cudaError_t launch_reject_inst(const SampleArgs& a, int B, int cs, int threads, cudaStream_t stream) {
-    auto kern = tree_reject_kernel<VEC, ALIGNED>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+static cudaError_t make_reject_config(int B, int cs, int threads, cudaStream_t stream, cudaLaunchConfig_t* cfg,
+                                      cudaLaunchAttribute* attr) {
+    cudaError_t e = cudaFuncSetAttribute(tree_reject_kernel<VEC, ALIGNED>,
+                                         cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(B * cs), 1, 1);
-    cfg.blockDim = dim3((unsigned)threads, 1, 1);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    *cfg = cudaLaunchConfig_t{};
+    cfg->gridDim = dim3((unsigned)(B * cs), 1, 1);
+    cfg->blockDim = dim3((unsigned)threads, 1, 1);
+    cfg->dynamicSmemBytes = 0;
+    cfg->stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)cs;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    cfg->attrs = attr;
+    cfg->numAttrs = 1;
+    return cudaSuccess;
+}
+
+template <int VEC, bool ALIGNED>
+static cudaError_t launch_reject_inst(const SampleArgs& a, int B, int cs, int threads, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    cudaError_t e = make_reject_config<VEC, ALIGNED>(B, cs, threads, stream, &cfg, attr);
+    if (e != cudaSuccess) return e;
+    return cudaLaunchKernelEx(&cfg, tree_reject_kernel<VEC, ALIGNED>, a);
+}
+
+// How many clusters of this shape can be resident at once (cached per shape).
+template <int VEC, bool ALIGNED>
+static int resident_clusters(int cs, int threads) {
+    static std::mutex mu;
+    static std::map<std::pair<int, int>, int> cache;
+    std::lock_guard<std::mutex> lock(mu);
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const auto key = std::make_pair(dev * 64 + cs, threads);
+    auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    cudaLaunchConfig_t cfg;
+    cudaLaunchAttribute attr[1];
+    int n = 0;
+    if (make_reject_config<VEC, ALIGNED>(1, cs, threads, nullptr, &cfg, attr) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, tree_reject_kernel<VEC, ALIGNED>, &cfg) != cudaSuccess)
+        n = 0;
+    cache[key] = n;
+    return n;
+}
+
+static int vec_for(int V, int cs, int threads, int* vpc_out) {
+    int vpc = (V + cs - 1) / cs;
+    vpc = (vpc + 3) & ~3;
+    *vpc_out = vpc;
+    const int need = (vpc + threads * 4 - 1) / (threads * 4);
+    return need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : need <= 8 ? 8 : 0;
+}
+
+template <bool ALIGNED>
+static int resident_for(int vec, int cs, int threads) {
+    switch (vec) {
+        case 1: return resident_clusters<1, ALIGNED>(cs, threads);
+        case 2: return resident_clusters<2, ALIGNED>(cs, threads);
+        case 4: return resident_clusters<4, ALIGNED>(cs, threads);
+        default: return resident_clusters<8, ALIGNED>(cs, threads);
+    }
 }
 
 // Chooses the cluster size, block size and per-thread vector count for a vocabulary of
-// V entries and B sequences, then launches one cluster per sequence.
+// V entries and B sequences, then launches one cluster per sequence (16-CTA clusters
+// need 16 free SMs in one GPC, so their residency is checked).
 cudaError_t launch_tree_reject(SampleArgs a, int B, int num_sms, cudaStream_t stream) {
     if (B == 0) return cudaSuccess;
     const int V = a.V;
     int threads = 64;
     while (threads < 512 && threads * 4 * 2 < V) threads *= 2;
     const int cap1 = threads * 4 * 8;  // entries one CTA holds at VEC = 8
-    int cs = 1;
-    while (cs * cap1 < V) cs *= 2;  // smallest cluster that fits the row
-    if (V > threads * 4 * 2) {      // rows long enough to be worth splitting further
-        while (cs < 16 && B * cs * 2 <= 2 * num_sms) cs *= 2;
-    }
-    int vpc = (V + cs - 1) / cs;
-    vpc = (vpc + 3) & ~3;
-    a.v_per_cta = vpc;
-    const int need = (vpc + threads * 4 - 1) / (threads * 4);
+    int cs_min = 1;
+    while (cs_min * cap1 < V) cs_min *= 2;  // smallest cluster that fits the row
     const bool aligned = (V % 4) == 0 && (reinterpret_cast<uintptr_t>(a.logits) & 15) == 0 &&
                          (a.probs == nullptr || (reinterpret_cast<uintptr_t>(a.probs) & 15) == 0);
-    if (need <= 1) return aligned ? launch_reject_inst<1, true>(a, B, cs, threads, stream)
-                                  : launch_reject_inst<1, false>(a, B, cs, threads, stream);
-    if (need <= 2) return aligned ? launch_reject_inst<2, true>(a, B, cs, threads, stream)
-                                  : launch_reject_inst<2, false>(a, B, cs, threads, stream);
-    if (need <= 4) return aligned ? launch_reject_inst<4, true>(a, B, cs, threads, stream)
-                                  : launch_reject_inst<4, false>(a, B, cs, threads, stream);
-    if (need <= 8) return aligned ? launch_reject_inst<8, true>(a, B, cs, threads, stream)
-                                  : launch_reject_inst<8, false>(a, B, cs, threads, stream);
-    return cudaErrorInvalidValue;
+    // Enough CTAs that a thread holds at most 16 entries (VEC <= 4): longer rows per
+    // thread make every pass slower, more CTAs make every cluster barrier slower.  A
+    // larger cluster is kept only if all B clusters can be resident at once.
+    int cs = cs_min;
+    while (cs < 16 && cs * threads * 16 < V) cs *= 2;
+    while (cs > cs_min) {
+        int vpc;
+        const int vec = vec_for(V, cs, threads, &vpc);
+        const int res = aligned ? resident_for<true>(vec, cs, threads) : resident_for<false>(vec, cs, threads);
+        if (res >= B && B * cs <= 2 * num_sms) break;
+        cs >>= 1;
+    }
+    int vpc;
+    const int vec = vec_for(V, cs, threads, &vpc);
+    a.v_per_cta = vpc;
+    switch (vec) {
+        case 1: return aligned ? launch_reject_inst<1, true>(a, B, cs, threads, stream)
+                               : launch_reject_inst<1, false>(a, B, cs, threads, stream);
+        case 2: return aligned ? launch_reject_inst<2, true>(a, B, cs, threads, stream)
+                               : launch_reject_inst<2, false>(a, B, cs, threads, stream);
+        case 4: return aligned ? launch_reject_inst<4, true>(a, B, cs, threads, stream)
+                               : launch_reject_inst<4, false>(a, B, cs, threads, stream);
+        case 8: return aligned ? launch_reject_inst<8, true>(a, B, cs, threads, stream)
+                               : launch_reject_inst<8, false>(a, B, cs, threads, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace tsv
