@@ -19,7 +19,9 @@
 //   warps 4-11  softmax, one thread per query row (warpgroup m owns M tile m): reads
 //               its S row from TMEM, applies the prefix/ancestor mask, keeps a running
 //               max (rescaling O in TMEM only when the max grows by more than 2^8) and
-//               sum, writes P (bf16) into shared memory for the PV product.
+//               sum, writes P (bf16 pairs) back into TMEM over the S columns it has
+//               read; the PV MMA takes P as its TMEM A operand, so shared memory holds
+//               only Q and the K/V ring (5 slots of 128 keys at D = 128, two M tiles).
 // Sequences whose prefix spans several chunks write (m, l, O / l) partials that the
 // merge kernel combines; single-chunk sequences write the output directly.
 // Every mbarrier wait is bounded (about one second); a timeout sets TSV_DERR_TIMEOUT
@@ -36,9 +38,8 @@ namespace {
 
 constexpr int kThreads = 384;
 constexpr int kTileKeys = 128;
-constexpr uint32_t kPBytes = 128 * 128 * 2;  // one P tile (128 rows x 128 keys, bf16)
 constexpr uint32_t kHalfBytes = 128 * 128;   // 128 rows x 64 bf16 (one 128B-swizzled half)
-constexpr int kMaxSlots = 8;
+constexpr int kMaxSlots = 12;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
 
 // ----------------------------------------------------------------------------- PTX wrappers
@@ -113,6 +114,16 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint6
         "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
             d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// D[tmem] (+)= A[tmem] * B[smem desc]: A (M x K bf16) read from TMEM, lane = row,
+// two K-consecutive elements per 32-bit column (lower half = lower k)
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\ntcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(
+            d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 // arrives on `bar` once every tcgen05 operation issued so far by this thread is complete
@@ -191,27 +202,21 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int q) {
 }
 
 struct TcLayout {
-    uint32_t q0, p0, ring, bars, misc, total;
+    uint32_t q0, ring, bars, misc, total;
     int slots;
 };
 
 template <int D>
 __host__ __device__ inline TcLayout tc_layout(int nm_max) {
+    // Q tiles (one per M tile) | ring of K/V slots | barriers | parents.  P lives in TMEM.
     TcLayout L{};
     const uint32_t qbytes = 128u * D * 2u, slot = 128u * D * 2u;
     L.q0 = 0;
-    L.p0 = 2 * qbytes;
-    L.ring = L.p0 + 2 * kPBytes;
+    L.ring = (nm_max == 2 ? 2u : 1u) * qbytes;
     const uint32_t budget = 232448u - 1024u - 1024u;  // max dynamic smem - alignment slack - barriers/misc
-    const uint32_t used = nm_max == 2 ? L.ring : (qbytes + kPBytes);  // a single M tile leaves Q1/P1 unused
     int slots = static_cast<int>((budget - L.ring) / slot);
-    if (nm_max < 2) slots = static_cast<int>((budget - used) / slot);
     if (slots > kMaxSlots) slots = kMaxSlots;
     L.slots = slots;
-    if (nm_max < 2) {  // pack: Q0 | P0 | ring
-        L.p0 = qbytes;
-        L.ring = qbytes + kPBytes;
-    }
     L.bars = L.ring + slots * slot;
     L.misc = L.bars + 512;
     L.total = L.misc + 512 + 1024;
@@ -374,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idS = idesc_bf16(128, 128, false);
             constexpr uint32_t idO = idesc_bf16(128, D, true);
-            const uint32_t q_base = smem_u32(smem + lay.q0), p_base = smem_u32(smem + lay.p0);
+            const uint32_t q_base = smem_u32(smem + lay.q0);
             const uint32_t ring_base = smem_u32(smem + lay.ring);
             auto issue_S = [=](int m, int slot) {
                 const uint32_t qa = q_base + m * (128u * D * 2u);
@@ -386,15 +391,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                              k > 0);
                 }
             };
+            // P_m is in TMEM over S_m's columns (16 keys = 8 columns per MMA)
             auto issue_PV = [=](int m, int slot, bool acc_first) {
-                const uint32_t pa = p_base + m * kPBytes;
                 const uint32_t vb = ring_base + slot * SLOT;
 #pragma unroll
-                for (int k = 0; k < kTileKeys / 16; ++k) {
-                    const uint32_t aoff = (k >> 2) * kHalfBytes + (k & 3) * 32;
-                    mma_bf16(tmem + 256 + m * D, sdesc_sw128(pa + aoff, 16, 1024),
-                             sdesc_sw128(vb + k * 16 * 128, kHalfBytes, 1024), idO, (acc_first || k > 0) ? 1u : 0u);
-                }
+                for (int k = 0; k < kTileKeys / 16; ++k)
+                    mma_bf16_ts(tmem + 256 + m * D, tmem + m * 128 + k * 8,
+                                sdesc_sw128(vb + k * 16 * 128, kHalfBytes, 1024), idO, (acc_first || k > 0) ? 1u : 0u);
             };
             bool ok = mbar_wait(bar(Bars::kQ), 0, s_abort);
             tc_fence_after();
@@ -484,7 +487,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + lane_base + wg * 128;
         const uint32_t tO = tmem + lane_base + 256 + wg * D;
-        uint8_t* pt = smem + lay.p0 + wg * kPBytes;
         float m_run = -INFINITY, l_run = 0.0f;
         const float sl2 = a.scale_log2;
         bool ok = true;
@@ -590,21 +592,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int cc = 0; cc < 32; ++cc) pa[cc] = pb[cc] = 0u;
                     }
+                    // pack to bf16 pairs and store over the S columns already read
+                    uint32_t w[32];
 #pragma unroll
-                    for (int q8 = 0; q8 < 8; ++q8) {
-                        uint32_t w[4];
-#pragma unroll
-                        for (int e2 = 0; e2 < 4; ++e2) {
-                            const int cc = (q8 & 3) * 8 + 2 * e2;
-                            const float p0 = __uint_as_float(q8 < 4 ? pa[cc] : pb[cc]);
-                            const float p1 = __uint_as_float(q8 < 4 ? pa[cc + 1] : pb[cc + 1]);
-                            la[e2] += p0 + p1;
-                            __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
-                            w[e2] = *reinterpret_cast<uint32_t*>(&pk);
-                        }
-                        *reinterpret_cast<uint4*>(pt + sw128_offset(tw, h2 * 8 + q8)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    for (int i = 0; i < 32; ++i) {
+                        const float p0 = __uint_as_float(i < 16 ? pa[2 * i] : pb[2 * i - 32]);
+                        const float p1 = __uint_as_float(i < 16 ? pa[2 * i + 1] : pb[2 * i - 31]);
+                        la[i & 3] += p0 + p1;
+                        __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
+                        w[i] = *reinterpret_cast<uint32_t*>(&pk);
                     }
+                    tmem_st32(tS + h2 * 32, w);
                 }
+                tmem_wait_st();
                 l_run += (la[0] + la[1]) + (la[2] + la[3]);
             }
             // the last tile's V rows past the key range are zeroed before the PV product
@@ -624,7 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            fence_proxy_async_smem();
+            fence_proxy_async_smem();  // the zeroed V rows, written through the generic proxy
             tc_fence_before();
             mbar_arrive(bar(Bars::kP + wg));
             if (!ok) break;
