@@ -15,7 +15,8 @@
 //               (cache block, 64-wide half of D), 128B-swizzled, into a ring of slots;
 //   warp 1      TMEM owner and MMA issuer: S_m = Q_m K^T (128 x 128, fp32 in TMEM) and
 //               O_m += P_m V (128 x D, fp32 in TMEM), ping-ponging the two M tiles so
-//               one tile's softmax overlaps the other tile's MMAs;
+//               one tile's softmax overlaps the other tile's MMAs (with a single M tile,
+//               S is double-buffered across key tiles instead);
 //   warps 4-11  softmax, one thread per query row (warpgroup m owns M tile m): reads
 //               its S row from TMEM, applies the prefix/ancestor mask, keeps a running
 //               max (rescaling O in TMEM only when the max grows by more than 2^8) and
@@ -381,59 +382,94 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idO = idesc_bf16(128, D, true);
             const uint32_t q_base = smem_u32(smem + lay.q0);
             const uint32_t ring_base = smem_u32(smem + lay.ring);
-            auto issue_S = [=](int m, int slot) {
-                const uint32_t qa = q_base + m * (128u * D * 2u);
+            // S buffer sb (TMEM columns sb*128) = Q tile qm . K^T
+            auto issue_S = [=](int qm, int sb, int slot) {
+                const uint32_t qa = q_base + qm * (128u * D * 2u);
                 const uint32_t kb = ring_base + slot * SLOT;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
                     const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-                    mma_bf16(tmem + m * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idS,
+                    mma_bf16(tmem + sb * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idS,
                              k > 0);
                 }
             };
-            // P_m is in TMEM over S_m's columns (16 keys = 8 columns per MMA)
-            auto issue_PV = [=](int m, int slot, bool acc_first) {
+            // O tile om += P . V, P in TMEM over S buffer pb's columns (16 keys = 8 columns per MMA)
+            auto issue_PV = [=](int om, int pb, int slot, bool acc_first) {
                 const uint32_t vb = ring_base + slot * SLOT;
 #pragma unroll
                 for (int k = 0; k < kTileKeys / 16; ++k)
-                    mma_bf16_ts(tmem + 256 + m * D, tmem + m * 128 + k * 8,
+                    mma_bf16_ts(tmem + 256 + om * D, tmem + pb * 128 + k * 8,
                                 sdesc_sw128(vb + k * 16 * 128, kHalfBytes, 1024), idO, (acc_first || k > 0) ? 1u : 0u);
             };
             bool ok = mbar_wait(bar(Bars::kQ), 0, s_abort);
             tc_fence_after();
-            // prologue: S_m(0)
-            ok = ok && mbar_wait(bar(Bars::kFull + 0), 0, s_abort);
-            tc_fence_after();
-            if (ok) {
-                for (int m = 0; m < nm; ++m) {
-                    issue_S(m, 0);
-                    mma_commit(bar(Bars::kS + m));
-                }
-                mma_commit(bar(Bars::kEmpty + 0));
-            }
-            for (int j = 0; j < ntiles && ok; ++j) {
-                const int fV = 2 * j + 1, fK = 2 * j + 2;
-                ok = mbar_wait(bar(Bars::kFull + fV % nslots), (fV / nslots) & 1, s_abort);
+            if (nm == 2) {
+                // two M tiles ping-pong: one tile's softmax overlaps the other's MMAs
+                ok = ok && mbar_wait(bar(Bars::kFull + 0), 0, s_abort);
                 tc_fence_after();
-                for (int m = 0; m < nm && ok; ++m) {
-                    ok = mbar_wait(bar(Bars::kP + m), j & 1, s_abort);
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_PV(m, fV % nslots, j > 0);
-                    mma_commit(bar(Bars::kO + m));
-                    if (m == nm - 1) mma_commit(bar(Bars::kEmpty + fV % nslots));  // V_j's last reader issued
-                    if (j + 1 < ntiles) {
-                        if (m == 0) {
-                            ok = mbar_wait(bar(Bars::kFull + fK % nslots), (fK / nslots) & 1, s_abort);
-                            if (!ok) break;
-                            tc_fence_after();
-                        }
-                        issue_S(m, fK % nslots);
+                if (ok) {
+                    for (int m = 0; m < nm; ++m) {
+                        issue_S(m, m, 0);
                         mma_commit(bar(Bars::kS + m));
                     }
+                    mma_commit(bar(Bars::kEmpty + 0));
                 }
-                if (!ok) break;
-                if (j + 1 < ntiles) mma_commit(bar(Bars::kEmpty + fK % nslots));
+                for (int j = 0; j < ntiles && ok; ++j) {
+                    const int fV = 2 * j + 1, fK = 2 * j + 2;
+                    ok = mbar_wait(bar(Bars::kFull + fV % nslots), (fV / nslots) & 1, s_abort);
+                    tc_fence_after();
+                    for (int m = 0; m < nm && ok; ++m) {
+                        ok = mbar_wait(bar(Bars::kP + m), j & 1, s_abort);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_PV(m, m, fV % nslots, j > 0);
+                        mma_commit(bar(Bars::kO + m));
+                        if (m == nm - 1) mma_commit(bar(Bars::kEmpty + fV % nslots));  // V_j's last reader issued
+                        if (j + 1 < ntiles) {
+                            if (m == 0) {
+                                ok = mbar_wait(bar(Bars::kFull + fK % nslots), (fK / nslots) & 1, s_abort);
+                                if (!ok) break;
+                                tc_fence_after();
+                            }
+                            issue_S(m, m, fK % nslots);
+                            mma_commit(bar(Bars::kS + m));
+                        }
+                    }
+                    if (!ok) break;
+                    if (j + 1 < ntiles) mma_commit(bar(Bars::kEmpty + fK % nslots));
+                }
+            } else {
+                // one M tile: S is double-buffered across key tiles (tile j in buffer j & 1),
+                // so S(j+1) is computed while tile j's softmax runs.  K fills are consumed
+                // ahead of V fills (K0, K1, V0, K2, V1, ...); the ring holds >= 3 slots.
+                for (int jj = 0; jj < 2 && jj < ntiles && ok; ++jj) {
+                    const int fK = 2 * jj;
+                    ok = mbar_wait(bar(Bars::kFull + fK % nslots), (fK / nslots) & 1, s_abort);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_S(0, jj, fK % nslots);
+                    mma_commit(bar(Bars::kS + jj));
+                    mma_commit(bar(Bars::kEmpty + fK % nslots));
+                }
+                for (int j = 0; j < ntiles && ok; ++j) {
+                    const int b2 = j & 1;
+                    const int fV = 2 * j + 1, fK = 2 * j + 4;
+                    ok = mbar_wait(bar(Bars::kFull + fV % nslots), (fV / nslots) & 1, s_abort) &&
+                         mbar_wait(bar(Bars::kP + b2), (j >> 1) & 1, s_abort);
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_PV(0, b2, fV % nslots, j > 0);
+                    mma_commit(bar(Bars::kO + 0));
+                    mma_commit(bar(Bars::kEmpty + fV % nslots));
+                    if (j + 2 < ntiles) {
+                        ok = mbar_wait(bar(Bars::kFull + fK % nslots), (fK / nslots) & 1, s_abort);
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_S(0, b2, fK % nslots);  // after PV(j) has read P(j) from this buffer
+                        mma_commit(bar(Bars::kS + b2));
+                        mma_commit(bar(Bars::kEmpty + fK % nslots));
+                    }
+                }
             }
             if (!ok) my_err = 1;
             // drain: every issued MMA completes before TMEM is released
@@ -485,14 +521,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const bool warp_active = __any_sync(0xffffffffu, valid) && (wg < nm);
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tS = tmem + lane_base + wg * 128;
+        const uint32_t tS0 = tmem + lane_base;
         const uint32_t tO = tmem + lane_base + 256 + wg * D;
         float m_run = -INFINITY, l_run = 0.0f;
         const float sl2 = a.scale_log2;
         bool ok = true;
         for (int j = 0; j < ntiles && wg < nm; ++j) {
             const int t0 = k_begin + j * kTileKeys;
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(Bars::kS + wg), j & 1, s_abort));
+            // S/P buffer of this tile: the warpgroup's own with two M tiles; alternating
+            // buffers (double-buffered S) with one
+            const int sb = nm == 2 ? wg : (j & 1);
+            const uint32_t sphase = nm == 2 ? (j & 1) : ((j >> 1) & 1);
+            const uint32_t tS = tS0 + sb * 128;
+            ok = __all_sync(0xffffffffu, mbar_wait(bar(Bars::kS + sb), sphase, s_abort));
             if (!ok) break;
             tc_fence_after();
             if (warp_active) {
@@ -626,7 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             fence_proxy_async_smem();  // the zeroed V rows, written through the generic proxy
             tc_fence_before();
-            mbar_arrive(bar(Bars::kP + wg));
+            mbar_arrive(bar(Bars::kP + sb));
             if (!ok) break;
         }
         // epilogue: O / l
