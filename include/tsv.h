@@ -84,10 +84,13 @@ const char *tsv_last_error(void);
  * q, caches and out share `dtype` (bf16: tensor-core tiles, fp32 accumulation;
  * fp32: exact fp32 FMA path).  D in {64, 128}; 1 <= N <= 128; Hq % Hkv == 0;
  * block_size a power of two in [8, 128].
- * Long prefixes are split into key chunks whose partial (max, sum, output) go to
- * `workspace` and are merged by a second kernel; `workspace` must hold
- * tsv_attn_workspace_size(...) bytes (may be NULL when that is 0) and is
- * scratch owned by the caller, not read before it is written.
+ * bf16: persistent CTAs split the 128-key tiles of all (sequence, kv head) pairs
+ * evenly; a pair that straddles CTAs leaves partial (max, sum, output) in
+ * `workspace`, merged by the CTA that finishes its last piece.  fp32: long prefixes
+ * are split into key chunks whose partials are merged by a second kernel.
+ * `workspace` must hold tsv_attn_workspace_size(...) bytes (may be NULL when that
+ * is 0); it is scratch owned by the caller, and every byte the call reads there is
+ * written earlier in the same call (no clearing needed between calls).
  * Rows of a sequence with seq_err != 0 are written as NaN.
  * Cache slots from L_b + N to the end of the sequence's last block are never
  * read into the result (they may hold anything, NaN included).
@@ -110,7 +113,7 @@ tsv_status tsv_tree_verify_attn(const void *q, const void *k_cache, const void *
  * that owns all device memory and passes only inputs and outputs, or a loop that
  * must not call cudaMalloc because it can synchronise the device.  Same arguments
  * and result as tsv_tree_verify_attn, minus the workspace: the split-K partials go
- * to a scratch array of tsv_noalloc_scratch_bytes() (32 MiB) that the library
+ * to a scratch array of tsv_noalloc_scratch_bytes() (64 MiB) that the library
  * defines in device memory; every GPU that loads the library holds it until the
  * process exits.  Nothing is allocated per call.
  *  - Shapes whose tsv_attn_workspace_size exceeds the array are rejected with

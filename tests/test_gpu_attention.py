@@ -62,6 +62,19 @@ def test_bad_sequences_are_poisoned_and_flagged():
     _check_all_rows(inp)
 
 
+def test_many_units_two_row_groups_flagged_in_the_middle():
+    # 12 sequences of mixed lengths (empty prefixes included) cut across CTAs; 320 rows
+    # per kv head = a full and a partial row group; two flagged sequences mid-batch
+    w = W.CONFIGS[3].replace(B=12, Hq=32, Hkv=4, N=40, depth=6, prefix=(0, 2600), V=64, seed=91)
+    inp = W.generate(w)
+    inp["seq_lens"] = inp["seq_lens"].copy()
+    inp["seq_lens"][3] = 0
+    inp["seq_lens"][5] = -7
+    inp["block_table"] = inp["block_table"].copy()
+    inp["block_table"][8, 0] = -1
+    _check_all_rows(inp)
+
+
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4])
 def test_full_size_sampled_rows(cfg):
     inp = W.generate(W.CONFIGS[cfg])

@@ -57,15 +57,16 @@ def test_no_alloc_refuses_shapes_beyond_its_scratch():
     B, N, Hq, D = d["q"].shape
     lib = tsv.load()
     cap = lib.tsv_noalloc_scratch_bytes()
-    big_blocks = 1 << 20  # a block table wide enough that the planned scratch exceeds the array
-    need = tsv.attn_workspace_size(B, N, Hq, inp["Hkv"], D, 16, big_blocks, tsv.TSV_BF16)
+    # fp32 key chunks: a block table wide enough that the planned scratch exceeds the array
+    big_blocks = 1 << 20
+    need = tsv.attn_workspace_size(B, N, Hq, inp["Hkv"], D, 16, big_blocks, tsv.TSV_F32)
     assert need > cap
     out = torch.empty_like(d["q"])
     err = torch.empty(B, dtype=torch.int32, device="cuda")
     st = lib.tsv_tree_verify_attn_noalloc(d["q"].data_ptr(), d["k_cache"].data_ptr(), d["v_cache"].data_ptr(),
                                           d["block_table"].data_ptr(), d["seq_lens"].data_ptr(),
                                           d["parent"].data_ptr(), out.data_ptr(), B, N, Hq, inp["Hkv"], D, 16,
-                                          big_blocks, inp["num_blocks"], inp["scale"], tsv.TSV_BF16,
+                                          big_blocks, inp["num_blocks"], inp["scale"], tsv.TSV_F32,
                                           err.data_ptr(), torch.cuda.current_stream().cuda_stream)
     assert st == tsv.TSV_ERR_UNSUPPORTED
     assert b"scratch" in lib.tsv_last_error()

@@ -56,11 +56,12 @@ int log2i(int x) {
 bool use_tc(tsv_dtype dt, int D) { return dt == TSV_BF16 && tsv::attn_tc_supported(D); }  // D checked before
 
 tsv::AttnPlan plan_for(int B, int N, int Hq, int Hkv, int D, int block_size, int max_blocks, tsv_dtype dt) {
-    const bool tc = use_tc(dt, D);
-    // tensor-core work items hold a whole SM (TMEM, ~226 KB smem): about two waves of
-    // chunks of at least 512 keys; FMA items are small: eight waves of chunks >= 256
-    return tsv::make_attn_plan(B, N, Hq, Hkv, D, block_size, max_blocks,
-                               tc ? tsv::attn_tc_rows_per_cta() : 16, device_sms(), tc ? 2 : 8, tc ? 512 : 256);
+    // tensor-core path: persistent CTAs, one per SM, splitting all tiles evenly; FMA
+    // work items are small: eight waves of key chunks of at least 256 keys
+    if (use_tc(dt, D))
+        return tsv::make_attn_plan_tc(B, N, Hq, Hkv, D, block_size, max_blocks, tsv::attn_tc_rows_per_cta(),
+                                      device_sms());
+    return tsv::make_attn_plan(B, N, Hq, Hkv, D, block_size, max_blocks, 16, device_sms(), 8, 256);
 }
 
 tsv_status check_attn_shapes(int B, int N, int Hq, int Hkv, int D, int block_size, int max_blocks,
@@ -126,10 +127,15 @@ tsv_status tsv_tree_verify_attn(const void* q, const void* k_cache, const void* 
     a.seq_lens = seq_lens;
     a.parent = parent;
     a.out = out;
-    const size_t rows = (size_t)B * Hkv * p.max_chunks * p.R;
+    const bool tc = use_tc(dtype, D);
+    // partial rows: tensor-core path two slots per CTA, FMA path one per (b, g, chunk)
+    const size_t rows = tc ? 2 * (size_t)p.lanes * p.n_rgroups * p.rows_item : (size_t)B * Hkv * p.max_chunks * p.R;
     a.part_o = static_cast<float*>(workspace);
     a.part_m = p.ws_bytes ? a.part_o + rows * D : nullptr;
     a.part_l = p.ws_bytes ? a.part_m + rows : nullptr;
+    a.unit_info = (tc && p.ws_bytes) ? reinterpret_cast<int*>(a.part_l + rows) : nullptr;
+    a.lanes = p.lanes;
+    a.rows_item = p.rows_item;
     a.seq_err = seq_err;
     a.B = B;
     a.N = N;
@@ -148,12 +154,12 @@ tsv_status tsv_tree_verify_attn(const void* q, const void* k_cache, const void* 
     a.max_chunks = p.max_chunks;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e;
-    if (dtype == TSV_BF16) {
-        e = tsv::launch_attn_tc(a, s);
+    if (tc) {
+        e = tsv::launch_attn_tc(a, s);  // check kernel, persistent kernel, merge kernel
     } else {
         e = tsv::launch_attn_simt_f32(a, s);
+        if (e == cudaSuccess) e = tsv::launch_attn_merge(a, false, s);
     }
-    if (e == cudaSuccess) e = tsv::launch_attn_merge(a, dtype == TSV_BF16, s);
     if (e != cudaSuccess) return cuda_fail(e, "tree_verify_attn launch");
     return TSV_OK;
 }

@@ -1,13 +1,21 @@
-// attn_common.cuh -- launch plan and shared arguments of the tree-attention kernels.
+// attn_common.cuh -- launch plans and shared arguments of the tree-attention kernels.
 //
-// Work decomposition (both the fp32 FMA path and the bf16 tensor-core path):
-// one work item = (sequence b, kv head g, key chunk c, row group).  The rows of a
-// (b, g) pair are the R = N * Gq query rows (node n, head h = g*Gq + j) ordered
-// n-major, so one GQA group shares every K/V tile it loads.  The prefix of
-// sequence b is cut into nchunks(b) = max(1, ceil(L_b / chunk)) key chunks; the
-// last chunk also carries the N tree keys.  A sequence with one chunk writes its
-// output directly; otherwise each chunk writes (m, l, O/l) partials to the
+// The rows of a (sequence b, kv head g) pair are the R = N * Gq query rows (node n,
+// head h = g*Gq + j) ordered n-major, so one GQA group shares every K/V tile it
+// loads; a row group holds up to rows_per_cta of them.
+//
+// fp32 FMA path (make_attn_plan): one work item = (b, g, key chunk c, row group).
+// The prefix of sequence b is cut into nchunks(b) = max(1, ceil(L_b / chunk)) key
+// chunks; the last chunk also carries the N tree keys.  A sequence with one chunk
+// writes its output directly; otherwise each chunk writes (m, l, O/l) partials to the
 // workspace and the merge kernel combines them (log-sum-exp), one warp per row.
+//
+// bf16 tensor-core path (make_attn_plan_tc): persistent CTAs, `lanes` per row group.
+// The keys [0, L_b + N) of every (b, g) unit are cut into 128-key tiles; all units'
+// tiles, b-major, form one sequence that is split evenly between the lanes, so every
+// CTA streams the same number of K/V tiles whatever the mix of lengths.  A unit that
+// straddles lanes leaves (m, l, O/l) partials in per-CTA slots, and a merge kernel over
+// all SMs combines them.
 #pragma once
 
 #include <cstddef>
@@ -23,6 +31,8 @@ struct AttnPlan {
     int chunk;         // prefix keys per chunk (multiple of 128)
     int max_chunks;    // upper bound of nchunks(b) from the block-table capacity
     size_t ws_bytes;   // partials workspace (0 when max_chunks == 1)
+    int lanes;         // tensor-core path: persistent CTAs per row group
+    int rows_item;     // tensor-core path: rows of a partial slot, min(R, rows_per_cta)
 };
 
 // Deterministic function of the shapes and the SM count (the workspace size query
@@ -52,6 +62,33 @@ inline AttnPlan make_attn_plan(int B, int N, int Hq, int Hkv, int D, int block_s
     return p;
 }
 
+// Tensor-core plan: one CTA per SM (as many lanes as fit beside the row groups), but
+// no fewer than about four tiles per CTA at the block table's capacity.  Workspace:
+// two partial slots per CTA (its first and its last unit may be pieces), then one
+// record per (b, g, row group) unit naming the lanes that hold its pieces.
+constexpr int kUnitInfoInts = 8;
+inline AttnPlan make_attn_plan_tc(int B, int N, int Hq, int Hkv, int D, int block_size, int max_blocks,
+                                  int rows_per_cta, int num_sms) {
+    AttnPlan p{};
+    p.G = Hq / Hkv;
+    p.R = N * p.G;
+    p.rows_per_cta = rows_per_cta;
+    p.n_rgroups = (p.R + rows_per_cta - 1) / rows_per_cta;
+    p.rows_item = p.R < rows_per_cta ? p.R : rows_per_cta;
+    const long long tiles_cap = (long long)B * Hkv * (((long long)max_blocks * block_size + 127) / 128);
+    long long lanes = num_sms / p.n_rgroups;
+    if (lanes < 1) lanes = 1;
+    if (lanes > (tiles_cap + 3) / 4) lanes = (tiles_cap + 3) / 4;
+    if (lanes < 1) lanes = 1;
+    p.lanes = (int)lanes;
+    p.chunk = 0;
+    p.max_chunks = 0;
+    const size_t slots = 2 * (size_t)p.lanes * p.n_rgroups;
+    p.ws_bytes = slots * p.rows_item * ((size_t)D + 2) * sizeof(float) +
+                 (size_t)B * Hkv * p.n_rgroups * kUnitInfoInts * sizeof(int);
+    return p;
+}
+
 struct AttnArgs {
     const void* q;
     const void* k_cache;
@@ -63,6 +100,9 @@ struct AttnArgs {
     float* part_o;  // [B][Hkv][max_chunks][R][D]
     float* part_m;  // [B][Hkv][max_chunks][R]
     float* part_l;  // [B][Hkv][max_chunks][R]
+    // tensor-core path: part_o [2 * CTAs][rows_item][D], part_m / part_l [2 * CTAs][rows_item]
+    int* unit_info;  // [B][Hkv][n_rgroups][8]: first lane, last lane, side of the first piece, -, T (int64)
+    int lanes, rows_item;
     int32_t* seq_err;
     int B, N, Hq, Hkv, D;
     int bs_log2, max_blocks, num_blocks;

@@ -11,9 +11,9 @@
 //
 // The array lives for as long as the library is loaded, on every GPU that loads
 // it.  All calls share it: two calls that overlap on the GPU (on different streams,
-// or from different host threads) race on it, so callers must order them.  The
-// partials written there are fully rewritten by each call before they are read,
-// so nothing in it needs clearing between calls.
+// or from different host threads) race on it, so callers must order them.  Every
+// byte a call reads there (partials, per-unit records) is written earlier in the same
+// call, so nothing in it needs clearing between calls.
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
@@ -28,7 +28,7 @@ tsv_status report_error(tsv_status s, const char* fmt, ...);
 
 namespace {
 
-constexpr size_t kScratchBytes = size_t(32) << 20;  // 32 MiB
+constexpr size_t kScratchBytes = size_t(64) << 20;  // 64 MiB
 constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_attn_scratch[kScratchBytes];

@@ -6,30 +6,42 @@
 // pass; each sees the cached prefix (attention_mask) and its own ancestors,
 // itself included (tree_attention_mask).
 //
-// One CTA = one work item (sequence b, kv head g, key chunk c, row group of up to
-// 256 query rows = two M=128 tiles).  The query rows of a kv head are the N * Gq
-// (node, head) pairs, so each K/V tile loaded from HBM feeds Gq * N rows.
+// Work split (persistent, stream-K style): the keys [0, L_b + N) of every unit
+// (sequence b, kv head g) are cut into 128-key tiles; the tiles of all units, b-major,
+// form one sequence that is cut evenly between `lanes` CTAs per row group, so every CTA
+// streams the same number of K/V tiles whatever the mix of prefix lengths.  The CTA of
+// row group rg handles query rows [256 rg, 256 rg + 256) of each unit (up to two M=128
+// tiles).  The query rows of a unit are the N * Gq (node, head) pairs, so each K/V tile
+// loaded from HBM feeds Gq * N rows.  A CTA walks its tiles as segments, one per unit
+// it touches; a segment that covers its whole unit writes the output directly, the
+// others write (m, l, O / l) partials to a per-CTA slot, which a merge kernel over all
+// SMs combines (log-sum-exp).  A small kernel run first checks every sequence (flags,
+// NaN rows); flagged sequences get no tiles.  The three kernels are chained with
+// programmatic dependent launch, so each one's launch and set-up overlap the tail of
+// the one before.
 //
 // Warp roles (384 threads):
 //   warp 0      TMA producer: 128-key K and V tiles of the paged cache, one box per
-//               (cache block, 64-wide half of D), 128B-swizzled, into a ring of slots;
+//               (cache block, 64-wide half of D), 128B-swizzled, into a ring of slots,
+//               running ahead across segment boundaries;
 //   warp 1      TMEM owner and MMA issuer: S_m = Q_m K^T (128 x 128, fp32 in TMEM) and
 //               O_m += P_m V (128 x D, fp32 in TMEM), ping-ponging the two M tiles so
 //               one tile's softmax overlaps the other tile's MMAs (with a single M tile,
 //               S is double-buffered across key tiles instead);
-//   warps 4-11  softmax, one thread per query row (warpgroup m owns M tile m): reads
-//               its S row from TMEM, applies the prefix/ancestor mask, keeps a running
-//               max (rescaling O in TMEM only when the max grows by more than 2^8) and
-//               sum, writes P (bf16 pairs) back into TMEM over the S columns it has
-//               read; the PV MMA takes P as its TMEM A operand, so shared memory holds
-//               only Q and the K/V ring (5 slots of 128 keys at D = 128, two M tiles).
-// Sequences whose prefix spans several chunks write (m, l, O / l) partials that the
-// merge kernel combines; single-chunk sequences write the output directly.
+//   warp 2      (set-up only) locates this CTA's first tile;
+//   warps 4-11  softmax, one thread per query row (warpgroup m owns M tile m): loads
+//               the segment's Q rows, reads its S row from TMEM, applies the prefix /
+//               ancestor mask, keeps a running max (rescaling O in TMEM only when the
+//               max grows by more than 2^8) and sum, writes P (bf16 pairs) back into
+//               TMEM over the S columns it has read; the PV MMA takes P as its TMEM A
+//               operand, so shared memory holds only Q and the K/V ring.
 // Every mbarrier wait is bounded (about one second); a timeout sets TSV_DERR_TIMEOUT
-// for the sequence, lets the other roles drain, frees TMEM and returns.
+// for the sequence being worked on, lets the other roles drain, frees TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
+
+#include <utility>
 
 #include "attn_common.cuh"
 #include "common.cuh"
@@ -202,6 +214,15 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int q) {
     return static_cast<uint32_t>(half * kHalfBytes + (row >> 3) * 1024 + (row & 7) * 128 + ((cc ^ (row & 7)) << 4));
 }
 
+// programmatic dependent launch: let the next kernel in the stream start launching /
+// wait until the previous kernel has completed and its writes are visible
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
 struct TcLayout {
     uint32_t q0, ring, bars, misc, total;
     int slots;
@@ -209,7 +230,7 @@ struct TcLayout {
 
 template <int D>
 __host__ __device__ inline TcLayout tc_layout(int nm_max) {
-    // Q tiles (one per M tile) | ring of K/V slots | barriers | parents.  P lives in TMEM.
+    // Q tiles (one per M tile) | ring of K/V slots | barriers | misc.  P lives in TMEM.
     TcLayout L{};
     const uint32_t qbytes = 128u * D * 2u, slot = 128u * D * 2u;
     L.q0 = 0;
@@ -231,15 +252,136 @@ struct Bars {
     static constexpr int kS = 2 * kMaxSlots;  // [2]
     static constexpr int kP = kS + 2;         // [2]
     static constexpr int kO = kP + 2;         // [2]
-    static constexpr int kQ = kO + 2;
+    static constexpr int kQ = kO + 2;         // one phase per segment
     static constexpr int kDone = kQ + 1;
     static constexpr int kCount = kDone + 1;
 };
 
+// misc region (512 bytes): parents of the segment's sequence (int8, two buffers by
+// segment parity), per-slot fill metadata, the CTA's schedule
+constexpr uint32_t kMiscPar = 0, kMiscMeta = 256, kMiscSched = 320;
+
+// Tiles of each unit of sequence b: 0 for a sequence the check kernel flagged (or
+// whose length does not fit the block table), else ceil((L_b + N) / 128).  The
+// timeout bit, which a CTA of this kernel may set while others read, is ignored, so
+// every thread sees the same schedule.
+__device__ __forceinline__ int seq_tiles(const AttnArgs& a, int b, int* L_out) {
+    const int L = __ldg(a.seq_lens + b);
+    const int e = a.seq_err[b] & ~TSV_DERR_TIMEOUT;
+    *L_out = L;
+    if (e != 0 || L < 0 || (long long)L + a.N > ((long long)a.max_blocks << a.bs_log2)) return 0;
+    return (L + a.N + kTileKeys - 1) / kTileKeys;
+}
+
+// Position in a CTA's run of tiles: unit (b, g), tile t of its Tb tiles, prefix L.
+struct TileIt {
+    int b, g, t, Tb, L;
+    // first tile of the next unit that has tiles (sequences without tiles are skipped)
+    __device__ __forceinline__ void next_unit(const AttnArgs& a) {
+        t = 0;
+        if (++g < a.Hkv) return;
+        g = 0;
+        do {
+            ++b;
+            Tb = b < a.B ? seq_tiles(a, b, &L) : 1;
+        } while (b < a.B && Tb == 0);
+    }
+    __device__ __forceinline__ void next(const AttnArgs& a) {
+        if (t + 1 < Tb)
+            ++t;
+        else
+            next_unit(a);
+    }
+};
+
+// lane owning global tile x when T tiles are cut into `lanes` runs [k T / lanes, (k+1) T / lanes)
+__device__ __forceinline__ int lane_of_tile(long long x, long long T, int lanes) {
+    return static_cast<int>(((x + 1) * lanes - 1) / T);
+}
+__device__ __forceinline__ long long lane_start(int k, long long T, int lanes) { return (long long)k * T / lanes; }
+
+// One warp: total tiles, this lane's run [s, e) and the unit/tile where it starts.
+// sched: b, g, t, Tb, L, count, s (2 words), T (2 words).
+__device__ __forceinline__ void find_start(const AttnArgs& a, int lane_c, int* sched) {
+    const int lane = threadIdx.x & 31;
+    long long T = 0;
+    for (int b0 = 0; b0 < a.B; b0 += 32) {
+        int L;
+        const int b = b0 + lane;
+        T += b < a.B ? seq_tiles(a, b, &L) : 0;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) T += __shfl_xor_sync(0xffffffffu, T, o);
+    T *= a.Hkv;
+    const long long s = lane_start(lane_c, T, a.lanes), e = lane_start(lane_c + 1, T, a.lanes);
+    int fb = 0, fg = 0, ft = 0, fTb = 1, fL = 0;
+    if (e > s) {
+        long long base = 0;
+        for (int b0 = 0; b0 < a.B; b0 += 32) {
+            int L = 0;
+            const int b = b0 + lane;
+            const int tb = b < a.B ? seq_tiles(a, b, &L) : 0;
+            const long long w = (long long)tb * a.Hkv;
+            long long incl = w;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const long long y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const long long excl = incl - w;
+            const unsigned hit = __ballot_sync(0xffffffffu, w > 0 && base + excl <= s && s < base + incl);
+            if (hit) {
+                const int src = __ffs(hit) - 1;
+                const long long off = s - (base + excl);
+                const int mg = static_cast<int>(off / (tb > 0 ? tb : 1)), mt = static_cast<int>(off % (tb > 0 ? tb : 1));
+                fb = __shfl_sync(0xffffffffu, b, src);
+                fg = __shfl_sync(0xffffffffu, mg, src);
+                ft = __shfl_sync(0xffffffffu, mt, src);
+                fTb = __shfl_sync(0xffffffffu, tb, src);
+                fL = __shfl_sync(0xffffffffu, L, src);
+                break;
+            }
+            base += __shfl_sync(0xffffffffu, incl, 31);
+        }
+    }
+    if (lane == 0) {
+        sched[0] = fb;
+        sched[1] = fg;
+        sched[2] = ft;
+        sched[3] = fTb;
+        sched[4] = fL;
+        sched[5] = static_cast<int>(e - s);
+        reinterpret_cast<long long*>(sched)[3] = s;  // words 6-7
+        reinterpret_cast<long long*>(sched)[4] = T;  // words 8-9
+    }
+}
+
+// One CTA per sequence, run before the attention kernel: the checks behind seq_err[b]
+// (capacity first; a parent array that is not a tree; a block id outside the cache)
+// and NaN rows for a flagged sequence.
+__global__ void __launch_bounds__(128) attn_tc_check_kernel(const AttnArgs a) {
+    __shared__ int s_flag;
+    pdl_launch_dependents();
+    const int b = blockIdx.x, N = a.N;
+    const int L = a.seq_lens[b];
+    const bool cap_ok = L >= 0 && (long long)L + N <= ((long long)a.max_blocks << a.bs_log2);
+    int e = cap_ok ? 0 : TSV_DERR_CAPACITY;
+    if (!block_tree_ok(a.parent + (long long)b * N, N, &s_flag)) e |= TSV_DERR_PARENT;
+    if (cap_ok)
+        e |= block_cache_errors(a.block_table + (long long)b * a.max_blocks, L, N, 1 << a.bs_log2, a.max_blocks,
+                                a.num_blocks, &s_flag);
+    if (threadIdx.x == 0) a.seq_err[b] = e;
+    if (e) {
+        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (long long)b * N * a.Hq * a.D;
+        const __nv_bfloat16 nan = __float2bfloat16_rn(__int_as_float(0x7fc00000));
+        for (long long i = threadIdx.x; i < (long long)N * a.Hq * a.D; i += blockDim.x) out[i] = nan;
+    }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_tc_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
-                   int nm_max) {
+    attn_tc_kernel(const __grid_constant__ AttnArgs a, const __grid_constant__ CUtensorMap tmk,
+                   const __grid_constant__ CUtensorMap tmv, int nm_max) {
     constexpr int HALVES = D / 64;
     constexpr uint32_t SLOT = 128u * D * 2u;
     extern __shared__ uint8_t smem_raw[];
@@ -247,65 +389,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const TcLayout lay = tc_layout<D>(nm_max);
     const int nslots = lay.slots;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + lay.bars);
-    int* s_par = reinterpret_cast<int*>(smem + lay.misc);  // [128]
+    int8_t* s_par = reinterpret_cast<int8_t*>(smem + lay.misc + kMiscPar);  // [2][128]
+    volatile int* s_meta = reinterpret_cast<volatile int*>(smem + lay.misc + kMiscMeta);  // [kMaxSlots]
+    int* s_sched = reinterpret_cast<int*>(smem + lay.misc + kMiscSched);
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + lay.bars + 8 * Bars::kCount);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + lay.bars + 8 * Bars::kCount + 4);
-    int* s_flag = reinterpret_cast<int*>(smem + lay.bars + 8 * Bars::kCount + 8);
     const uint32_t bar0 = smem_u32(bars);
     auto bar = [=](int i) { return bar0 + 8u * static_cast<uint32_t>(i); };
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.z, g = blockIdx.y;
-    const int mg = blockIdx.x % a.n_rgroups, c = blockIdx.x / a.n_rgroups;
-    const int L = a.seq_lens[b];
+    const int nrg = a.n_rgroups;
+    const int rg = blockIdx.x % nrg, lane_c = blockIdx.x / nrg;
     const int N = a.N;
-    const int32_t* bt = a.block_table + (long long)b * a.max_blocks;
-
-    // ---- validation (uniform).  Chunk-0 items check the whole sequence (they report
-    // errors and poison rows); other chunks check only what they read.
-    int e = 0;
     const int bs = 1 << a.bs_log2;
-    if ((long long)L < 0 || (long long)L + N > (long long)a.max_blocks * bs) e = TSV_DERR_CAPACITY;
-    const int nch = e ? 1 : num_chunks(L, a.chunk);
-    if (c >= nch) return;
-    const int k_begin = c * a.chunk;
-    const int k_end = (c == nch - 1) ? L + N : min(L, (c + 1) * a.chunk);
-    const bool has_tree = (c == nch - 1);
-    if (c == 0 || has_tree) {
-        if (!block_tree_ok(a.parent + (long long)b * N, N, s_flag)) e |= TSV_DERR_PARENT;
-    }
-    if (!(e & TSV_DERR_CAPACITY)) {
-        const int blk0 = (c == 0) ? 0 : (k_begin >> a.bs_log2);
-        const int blk1 = (c == 0) ? ((L + N + bs - 1) >> a.bs_log2) : ((k_end + bs - 1) >> a.bs_log2);
-        if (tid == 0) *s_flag = 0;
-        __syncthreads();
-        for (int j = blk0 + tid; j < blk1; j += blockDim.x) {
-            const int id = bt[j];
-            if (id < 0 || id >= a.num_blocks) *s_flag = TSV_DERR_BLOCK;
-        }
-        __syncthreads();
-        e |= *s_flag;
-        __syncthreads();
-    }
-    const int r_base = mg * 256;
+    const int r_base = rg * 256;
     const int nm = min(2, (a.R - r_base + 127) / 128);
-    if (e) {
-        if (c == 0) {
-            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out);
-            const int r1 = min(a.R, r_base + 256);
-            for (int idx = tid; idx < (r1 - r_base) * D; idx += blockDim.x) {
-                const int r = r_base + idx / D, d = idx % D;
-                const int n = r / a.G, h = g * a.G + r % a.G;
-                out[(((long long)b * N + n) * a.Hq + h) * D + d] = __float2bfloat16_rn(__int_as_float(0x7fc00000));
-            }
-            if (mg == 0 && g == 0 && tid == 0) a.seq_err[b] = e;
-        }
-        return;
-    }
-    if (c == 0 && mg == 0 && g == 0 && tid == 0) a.seq_err[b] = 0;
-    const int ntiles = (k_end - k_begin + kTileKeys - 1) / kTileKeys;
 
-    // ---- set-up: barriers, TMEM, parents
+    // ---- set-up: barriers, TMEM, where this CTA's tiles start
     if (tid == 0) {
         for (int i = 0; i < nslots; ++i) {
             mbar_init(bar(Bars::kFull + i), 1);
@@ -316,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bar(Bars::kP + m), 128);
             mbar_init(bar(Bars::kO + m), 1);
         }
-        mbar_init(bar(Bars::kQ), 256);
+        mbar_init(bar(Bars::kQ), 128 * nm);
         mbar_init(bar(Bars::kDone), 1);
         *s_abort = 0;
         fence_barrier_init();
@@ -325,59 +425,77 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(s_tmem), 512);
         tmem_relinquish();
     }
-    if (has_tree)
-        for (int i = tid; i < N; i += blockDim.x) s_par[i] = a.parent[(long long)b * N + i];
+    pdl_launch_dependents();
+    pdl_wait();  // seq_err comes from the check kernel
+    if (warp == 2) find_start(a, lane_c, s_sched);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *s_tmem;
+    const int count = s_sched[5];  // tiles of this CTA
+    const TileIt it0{s_sched[0], s_sched[1], s_sched[2], s_sched[3], s_sched[4]};
     int my_err = 0;
+    int err_b = it0.b;  // sequence flagged if a wait of this thread gives up
 
     if (warp == 0) {
         // ============================ TMA producer (whole warp: lane j loads the id of
-        // the tile's j-th cache block and issues that block's boxes, so a tile's block
-        // ids are fetched in one coalesced load instead of one dependent load each)
-        const int nfills = 2 * ntiles;
-        // block id of this lane's cache block for fill f (K and V fills of a tile share ids);
-        // loaded before waiting for the fill's slot so the load latency is hidden
-        auto tile_block = [=](int f) -> int {
-            const int t0 = k_begin + (f >> 1) * kTileKeys;
-            const int nb = (min(t0 + kTileKeys, k_end) - t0 + bs - 1) >> a.bs_log2;
-            return lane < nb ? bt[(t0 >> a.bs_log2) + lane] : 0;
-        };
-        int blk_next = tile_block(0);
-        for (int f = 0; f < nfills && !my_err; ++f) {
-            const int slot = f % nslots, use = f / nslots;
-            const int blk = blk_next;
-            if (f + 1 < nfills) blk_next = ((f + 1) >> 1) == (f >> 1) ? blk : tile_block(f + 1);
-            if (use > 0 && !__all_sync(0xffffffffu, mbar_wait(bar(Bars::kEmpty + slot), (use - 1) & 1, s_abort))) {
-                my_err = 1;
-                break;
+        // the tile's j-th cache block and issues that block's boxes).  The next tile's
+        // block ids are loaded while the current tile's fills wait for their slots.
+        TileIt it = it0;
+        int blk = 0;
+        if (count > 0) {
+            const int u0 = it.t * kTileKeys;
+            const int nb = (min(u0 + kTileKeys, it.L + N) - u0 + bs - 1) >> a.bs_log2;
+            blk = lane < nb ? __ldg(a.block_table + (long long)it.b * a.max_blocks + (u0 >> a.bs_log2) + lane) : 0;
+        }
+        int seg = 0;
+        for (int jt = 0; jt < count && !my_err; ++jt) {
+            if (jt > 0 && it.t == 0) ++seg;
+            const bool first = (jt == 0) || (it.t == 0);
+            const int t0 = it.t * kTileKeys;
+            const int nblk = (min(t0 + kTileKeys, it.L + N) - t0 + bs - 1) >> a.bs_log2;
+            const int g = it.g;
+            const int blk_cur = blk;
+            err_b = it.b;
+            if (jt + 1 < count) {
+                it.next(a);
+                const int u0 = it.t * kTileKeys;
+                const int nb = (min(u0 + kTileKeys, it.L + N) - u0 + bs - 1) >> a.bs_log2;
+                blk = lane < nb ? __ldg(a.block_table + (long long)it.b * a.max_blocks + (u0 >> a.bs_log2) + lane) : 0;
             }
-            const int t0 = k_begin + (f >> 1) * kTileKeys;
-            const int t1 = min(t0 + kTileKeys, k_end);
-            const int nblk = (t1 - t0 + bs - 1) >> a.bs_log2;
-            const CUtensorMap* map = (f & 1) ? &tmv : &tmk;
-            const uint32_t dst = smem_u32(smem + lay.ring + slot * SLOT);
-            if (lane == 0) mbar_expect_tx(bar(Bars::kFull + slot), static_cast<uint32_t>(nblk * bs * 128 * HALVES));
-            __syncwarp();
-            if (lane < nblk) {  // a 128-key tile spans at most 128 / 8 = 16 blocks
+#pragma unroll 1
+            for (int kv = 0; kv < 2; ++kv) {
+                const int f = 2 * jt + kv;
+                const int slot = f % nslots, use = f / nslots;
+                if (use > 0 && !__all_sync(0xffffffffu, mbar_wait(bar(Bars::kEmpty + slot), (use - 1) & 1, s_abort))) {
+                    my_err = 1;
+                    break;
+                }
+                const CUtensorMap* map = kv ? &tmv : &tmk;
+                const uint32_t dst = smem_u32(smem + lay.ring + slot * SLOT);
+                if (lane == 0) {
+                    if (kv == 0) s_meta[slot] = (seg << 1) | (first ? 1 : 0);  // read by the MMA issuer
+                    mbar_expect_tx(bar(Bars::kFull + slot), static_cast<uint32_t>(nblk * bs * 128 * HALVES));
+                }
+                __syncwarp();
+                if (lane < nblk) {  // a 128-key tile spans at most 128 / 8 = 16 blocks
 #pragma unroll
-                for (int hh = 0; hh < HALVES; ++hh)
-                    tma_load_3d(dst + hh * kHalfBytes + lane * bs * 128, map, bar(Bars::kFull + slot), hh * 64, g,
-                                blk * bs);
+                    for (int hh = 0; hh < HALVES; ++hh)
+                        tma_load_3d(dst + hh * kHalfBytes + lane * bs * 128, map, bar(Bars::kFull + slot), hh * 64, g,
+                                    blk_cur * bs);
+                }
             }
         }
         // never leave with copies in flight: wait for the latest fill of every slot
         if (lane == 0) {
-            for (int f = max(0, 2 * ntiles - nslots); f < 2 * ntiles; ++f) {
+            for (int f = max(0, 2 * count - nslots); f < 2 * count; ++f) {
                 volatile int never = 0;
                 if (!mbar_wait(bar(Bars::kFull + f % nslots), (f / nslots) & 1, &never)) my_err = 1;
             }
         }
     } else if (warp == 1) {
         // ============================ MMA issuer
-        if (lane == 0) {
+        if (lane == 0 && count > 0) {
             constexpr uint32_t idS = idesc_bf16(128, 128, false);
             constexpr uint32_t idO = idesc_bf16(128, D, true);
             const uint32_t q_base = smem_u32(smem + lay.q0);
@@ -401,12 +519,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_bf16_ts(tmem + 256 + om * D, tmem + pb * 128 + k * 8,
                                 sdesc_sw128(vb + k * 16 * 128, kHalfBytes, 1024), idO, (acc_first || k > 0) ? 1u : 0u);
             };
-            bool ok = mbar_wait(bar(Bars::kQ), 0, s_abort);
-            tc_fence_after();
+            // K tile of CTA tile jt in its slot; a tile that starts a segment also waits
+            // for that segment's Q.  *first = the tile starts a segment.
+            int q_seg = -1;
+            auto wait_K = [&](int jt, bool* first) -> bool {
+                const int f = 2 * jt;
+                if (!mbar_wait(bar(Bars::kFull + f % nslots), (f / nslots) & 1, s_abort)) return false;
+                const int meta = s_meta[f % nslots];
+                *first = (meta & 1) != 0;
+                const int sg = meta >> 1;
+                if (sg != q_seg) {
+                    if (!mbar_wait(bar(Bars::kQ), sg & 1, s_abort)) return false;
+                    q_seg = sg;
+                }
+                tc_fence_after();
+                return true;
+            };
+            bool ok = true;
             if (nm == 2) {
                 // two M tiles ping-pong: one tile's softmax overlaps the other's MMAs
-                ok = ok && mbar_wait(bar(Bars::kFull + 0), 0, s_abort);
-                tc_fence_after();
+                bool fcur = false;
+                ok = wait_K(0, &fcur);
                 if (ok) {
                     for (int m = 0; m < nm; ++m) {
                         issue_S(m, m, 0);
@@ -414,60 +547,65 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     mma_commit(bar(Bars::kEmpty + 0));
                 }
-                for (int j = 0; j < ntiles && ok; ++j) {
-                    const int fV = 2 * j + 1, fK = 2 * j + 2;
+                for (int jt = 0; jt < count && ok; ++jt) {
+                    const int fV = 2 * jt + 1, fK = 2 * jt + 2;
                     ok = mbar_wait(bar(Bars::kFull + fV % nslots), (fV / nslots) & 1, s_abort);
                     tc_fence_after();
+                    bool fnext = false;
                     for (int m = 0; m < nm && ok; ++m) {
-                        ok = mbar_wait(bar(Bars::kP + m), j & 1, s_abort);
+                        ok = mbar_wait(bar(Bars::kP + m), jt & 1, s_abort);
                         if (!ok) break;
                         tc_fence_after();
-                        issue_PV(m, m, fV % nslots, j > 0);
+                        issue_PV(m, m, fV % nslots, !fcur);
                         mma_commit(bar(Bars::kO + m));
-                        if (m == nm - 1) mma_commit(bar(Bars::kEmpty + fV % nslots));  // V_j's last reader issued
-                        if (j + 1 < ntiles) {
+                        if (m == nm - 1) mma_commit(bar(Bars::kEmpty + fV % nslots));  // V_jt's last reader issued
+                        if (jt + 1 < count) {
                             if (m == 0) {
-                                ok = mbar_wait(bar(Bars::kFull + fK % nslots), (fK / nslots) & 1, s_abort);
+                                ok = wait_K(jt + 1, &fnext);
                                 if (!ok) break;
-                                tc_fence_after();
                             }
                             issue_S(m, m, fK % nslots);
                             mma_commit(bar(Bars::kS + m));
                         }
                     }
                     if (!ok) break;
-                    if (j + 1 < ntiles) mma_commit(bar(Bars::kEmpty + fK % nslots));
+                    if (jt + 1 < count) mma_commit(bar(Bars::kEmpty + fK % nslots));
+                    fcur = fnext;
                 }
             } else {
-                // one M tile: S is double-buffered across key tiles (tile j in buffer j & 1),
-                // so S(j+1) is computed while tile j's softmax runs.  K fills are consumed
+                // one M tile: S is double-buffered across key tiles (tile jt in buffer jt & 1),
+                // so S(jt+1) is computed while tile jt's softmax runs.  K fills are consumed
                 // ahead of V fills (K0, K1, V0, K2, V1, ...); the ring holds >= 3 slots.
-                for (int jj = 0; jj < 2 && jj < ntiles && ok; ++jj) {
-                    const int fK = 2 * jj;
-                    ok = mbar_wait(bar(Bars::kFull + fK % nslots), (fK / nslots) & 1, s_abort);
+                bool f0 = false, f1 = false;  // the tile in S buffer 0 / 1 starts a segment
+                for (int jj = 0; jj < 2 && jj < count && ok; ++jj) {
+                    bool fl = false;
+                    ok = wait_K(jj, &fl);
                     if (!ok) break;
-                    tc_fence_after();
-                    issue_S(0, jj, fK % nslots);
+                    issue_S(0, jj, (2 * jj) % nslots);
                     mma_commit(bar(Bars::kS + jj));
-                    mma_commit(bar(Bars::kEmpty + fK % nslots));
+                    mma_commit(bar(Bars::kEmpty + (2 * jj) % nslots));
+                    if (jj) f1 = fl;
+                    else f0 = fl;
                 }
-                for (int j = 0; j < ntiles && ok; ++j) {
-                    const int b2 = j & 1;
-                    const int fV = 2 * j + 1, fK = 2 * j + 4;
+                for (int jt = 0; jt < count && ok; ++jt) {
+                    const int b2 = jt & 1;
+                    const int fV = 2 * jt + 1, fK = 2 * jt + 4;
                     ok = mbar_wait(bar(Bars::kFull + fV % nslots), (fV / nslots) & 1, s_abort) &&
-                         mbar_wait(bar(Bars::kP + b2), (j >> 1) & 1, s_abort);
+                         mbar_wait(bar(Bars::kP + b2), (jt >> 1) & 1, s_abort);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_PV(0, b2, fV % nslots, j > 0);
+                    issue_PV(0, b2, fV % nslots, !(b2 ? f1 : f0));
                     mma_commit(bar(Bars::kO + 0));
                     mma_commit(bar(Bars::kEmpty + fV % nslots));
-                    if (j + 2 < ntiles) {
-                        ok = mbar_wait(bar(Bars::kFull + fK % nslots), (fK / nslots) & 1, s_abort);
+                    if (jt + 2 < count) {
+                        bool fl = false;
+                        ok = wait_K(jt + 2, &fl);
                         if (!ok) break;
-                        tc_fence_after();
-                        issue_S(0, b2, fK % nslots);  // after PV(j) has read P(j) from this buffer
+                        issue_S(0, b2, fK % nslots);  // after PV(jt) has read P(jt) from this buffer
                         mma_commit(bar(Bars::kS + b2));
                         mma_commit(bar(Bars::kEmpty + fK % nslots));
+                        if (b2) f1 = fl;
+                        else f0 = fl;
                     }
                 }
             }
@@ -477,252 +615,422 @@ __global__ void __launch_bounds__(kThreads, 1)
             volatile int never = 0;
             if (!mbar_wait(bar(Bars::kDone), 0, &never)) my_err = 1;
         }
-    } else if (warp >= 4) {
-        // ============================ softmax warpgroups
+    } else if (warp >= 4 && (warp - 4) / 4 < nm) {
+        // ============================ softmax warpgroups (warpgroup wg < nm)
         const int wg = (warp - 4) >> 2;
-        const int tw = tid - 128 - wg * 128;  // TMEM lane = tile row handled by this thread
+        const int nthr = 128 * nm;           // softmax threads taking part
+        const int stid = tid - 128;          // 0 .. nthr-1
+        const int tw = stid - wg * 128;      // TMEM lane = tile row handled by this thread
         // A partial M tile deals its rows round-robin over the four 32-lane quadrants of
         // TMEM (tile row tw holds row 4*(tw%32) + tw/32), so all four softmax warps share
         // the work; a full tile keeps the identity order.
         const int rows_here = min(128, a.R - r_base - wg * 128);
         const int rl = rows_here < 128 ? 4 * (tw & 31) + (tw >> 5) : tw;
         const int r = r_base + wg * 128 + rl;
-        const bool valid = (wg < nm) && (rl < rows_here);
+        const bool valid = rl < rows_here;
         const int n = valid ? r / a.G : 0;
-        const int h = g * a.G + (valid ? r % a.G : 0);
-        // Q row -> swizzled shared tile
-        {
-            uint8_t* qt = smem + lay.q0 + wg * (128u * D * 2u);
-            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
-                                                              (((long long)b * N + n) * a.Hq + h) * D);
-            if (wg < nm) {
-#pragma unroll
-                for (int qq = 0; qq < D / 8; ++qq) {
-                    uint4 v = valid ? __ldg(src + qq) : make_uint4(0, 0, 0, 0);
-                    *reinterpret_cast<uint4*>(qt + sw128_offset(tw, qq)) = v;
-                }
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(bar(Bars::kQ));
-        }
-        // ancestor mask of this row's node (tree keys only)
-        uint32_t anc0 = 0u, anc1 = 0u, anc2 = 0u, anc3 = 0u;
-        if (valid && has_tree) {
-            int x = n;
-            for (int step = 0; step <= N && x >= 0 && x < N; ++step) {
-                const uint32_t bit = 1u << (x & 31);
-                const int w = x >> 5;
-                anc0 |= w == 0 ? bit : 0u;
-                anc1 |= w == 1 ? bit : 0u;
-                anc2 |= w == 2 ? bit : 0u;
-                anc3 |= w == 3 ? bit : 0u;
-                x = s_par[x];
-            }
-        }
-        const bool warp_active = __any_sync(0xffffffffu, valid) && (wg < nm);
+        const int hj = valid ? r % a.G : 0;  // head within the GQA group
+        const bool warp_active = __any_sync(0xffffffffu, valid);
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t tS0 = tmem + lane_base;
         const uint32_t tO = tmem + lane_base + 256 + wg * D;
-        float m_run = -INFINITY, l_run = 0.0f;
         const float sl2 = a.scale_log2;
+        const long long s_first = reinterpret_cast<const long long*>(s_sched)[3];  // global index of tile 0
+        const long long T_all = reinterpret_cast<const long long*>(s_sched)[4];
         bool ok = true;
-        for (int j = 0; j < ntiles && wg < nm; ++j) {
-            const int t0 = k_begin + j * kTileKeys;
-            // S/P buffer of this tile: the warpgroup's own with two M tiles; alternating
-            // buffers (double-buffered S) with one
-            const int sb = nm == 2 ? wg : (j & 1);
-            const uint32_t sphase = nm == 2 ? (j & 1) : ((j >> 1) & 1);
-            const uint32_t tS = tS0 + sb * 128;
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(Bars::kS + sb), sphase, s_abort));
-            if (!ok) break;
-            tc_fence_after();
-            if (warp_active) {
-                // Two passes over the S row in TMEM, 64 columns per wait: the raw max
-                // first, then P = 2^(s*scale - m) written as bf16 into the swizzled P
-                // tile.  Independent accumulators (8 for the max, 4 for the sum) keep the
-                // FMNMX/MUFU latency chains short; the masked path is taken only for
-                // tiles that reach past the prefix.
-                const bool full_tile = (t0 + kTileKeys <= L) && (t0 + kTileKeys <= k_end);
-                float mxa[8];
+
+        // Q rows of unit (bq, gq) -> this warpgroup's swizzled shared tile
+        auto load_q = [&](int bq, int gq) {
+            uint8_t* qt = smem + lay.q0 + wg * (128u * D * 2u);
+            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
+                                                              (((long long)bq * N + n) * a.Hq + gq * a.G + hj) * D);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) mxa[i] = -INFINITY;
+            for (int qq = 0; qq < D / 8; ++qq) {
+                uint4 v = valid ? __ldg(src + qq) : make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(qt + sw128_offset(tw, qq)) = v;
+            }
+            fence_proxy_async_smem();
+            mbar_arrive(bar(Bars::kQ));
+        };
+
+        TileIt it = it0;
+        int jt = 0, seg = 0;
+        if (count > 0) load_q(it.b, it.g);
+        while (jt < count) {
+            // ---- segment: tiles [t_first, t_first + ntl) of unit (b, g)
+            const int b = it.b, g = it.g, L = it.L, Tb = it.Tb, t_first = it.t;
+            const int ntl = min(Tb - t_first, count - jt);
+            const int k_end = L + N;
+            const bool whole = (t_first == 0) && (ntl == Tb);
+            const long long unit_first = s_first + jt - t_first;  // global index of the unit's tile 0
+            err_b = b;
+            if (t_first == 0 && stid == 0) {
+                // this lane holds the unit's first piece: record where its pieces are
+                int* ui = a.unit_info + (((long long)b * a.Hkv + g) * nrg + rg) * kUnitInfoInts;
+                ui[0] = lane_c;
+                ui[1] = lane_of_tile(unit_first + Tb - 1, T_all, a.lanes);
+                ui[2] = seg == 0 ? 0 : 1;
+                ui[3] = 0;
+                reinterpret_cast<long long*>(ui)[2] = T_all;
+            }
+            // ancestor mask of this row's node (tree keys only)
+            uint32_t anc0 = 0u, anc1 = 0u, anc2 = 0u, anc3 = 0u;
+            if ((long long)(t_first + ntl) * kTileKeys > L) {
+                int8_t* par = s_par + (seg & 1) * 128;
+                for (int i = stid; i < N; i += nthr) par[i] = static_cast<int8_t>(a.parent[(long long)b * N + i]);
+                named_bar_sync(1, nthr);
+                if (valid) {
+                    int x = n;
+                    for (int step = 0; step <= N && x >= 0 && x < N; ++step) {
+                        const uint32_t bit = 1u << (x & 31);
+                        const int w = x >> 5;
+                        anc0 |= w == 0 ? bit : 0u;
+                        anc1 |= w == 1 ? bit : 0u;
+                        anc2 |= w == 2 ? bit : 0u;
+                        anc3 |= w == 3 ? bit : 0u;
+                        x = par[x];
+                    }
+                }
+            }
+            float m_run = -INFINITY, l_run = 0.0f;
+            for (int i = 0; i < ntl; ++i, ++jt) {
+                if (!ok) continue;
+                const int t0 = (t_first + i) * kTileKeys;
+                // S/P buffer of this tile: the warpgroup's own with two M tiles; alternating
+                // buffers (double-buffered S) with one
+                const int sb = nm == 2 ? wg : (jt & 1);
+                const uint32_t sphase = nm == 2 ? (jt & 1) : ((jt >> 1) & 1);
+                const uint32_t tS = tS0 + sb * 128;
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(Bars::kS + sb), sphase, s_abort));
+                if (!ok) {
+                    *s_abort = 1;
+                    continue;
+                }
+                tc_fence_after();
+                if (warp_active) {
+                    // Two passes over the S row in TMEM, 64 columns per wait: the raw max
+                    // first, then P = 2^(s*scale - m) written as bf16 pairs over the S
+                    // columns.  Independent accumulators (8 for the max, 4 for the sum) keep
+                    // the FMNMX/MUFU latency chains short; the masked path is taken only for
+                    // tiles that reach past the prefix.
+                    const bool full_tile = (t0 + kTileKeys <= L);
+                    float mxa[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) mxa[q] = -INFINITY;
 #pragma unroll 1
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    uint32_t pa[32], pb[32];
-                    tmem_ld32(tS + h2 * 64, pa);
-                    tmem_ld32(tS + h2 * 64 + 32, pb);
-                    tmem_wait_ld();
-                    if (valid) {
-                        if (full_tile) {
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        uint32_t pa[32], pb[32];
+                        tmem_ld32(tS + h2 * 64, pa);
+                        tmem_ld32(tS + h2 * 64 + 32, pb);
+                        tmem_wait_ld();
+                        if (valid) {
+                            if (full_tile) {
+#pragma unroll
+                                for (int cc = 0; cc < 32; ++cc) {
+                                    mxa[cc & 7] = fmaxf(mxa[cc & 7], __uint_as_float(pa[cc]));
+                                    mxa[cc & 7] = fmaxf(mxa[cc & 7], __uint_as_float(pb[cc]));
+                                }
+                            } else {
+#pragma unroll
+                                for (int cc = 0; cc < 32; ++cc) {
+                                    const int c0 = h2 * 64 + cc;
+                                    if (key_visible(t0 + c0, k_end, L, anc0, anc1, anc2, anc3))
+                                        mxa[cc & 7] = fmaxf(mxa[cc & 7], __uint_as_float(pa[cc]));
+                                    if (key_visible(t0 + c0 + 32, k_end, L, anc0, anc1, anc2, anc3))
+                                        mxa[cc & 7] = fmaxf(mxa[cc & 7], __uint_as_float(pb[cc]));
+                                }
+                            }
+                        }
+                    }
+                    const float mx_raw = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
+                                               fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
+                    const float mx = mx_raw * sl2;  // scale > 0: max commutes with it
+                    // within a segment, the PV product of the previous tile must be done
+                    // before O is rescaled (a segment's first PV overwrites O)
+                    if (i > 0) {
+                        ok = __all_sync(0xffffffffu, mbar_wait(bar(Bars::kO + wg), (jt - 1) & 1, s_abort));
+                        tc_fence_after();
+                    }
+                    const float m_new = fmaxf(m_run, mx);
+                    bool rescale = false;
+                    float factor = 1.0f;
+                    if (m_run == -INFINITY) {
+                        m_run = m_new;
+                    } else if (m_new > m_run + 8.0f) {
+                        factor = ex2(m_run - m_new);
+                        m_run = m_new;
+                        rescale = true;
+                    }
+                    l_run *= factor;
+                    if (__any_sync(0xffffffffu, rescale) && ok) {
+#pragma unroll 1
+                        for (int q4 = 0; q4 < D / 32; ++q4) {
+                            uint32_t ov[32];
+                            tmem_ld32(tO + q4 * 32, ov);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int cc = 0; cc < 32; ++cc) ov[cc] = __float_as_uint(__uint_as_float(ov[cc]) * factor);
+                            tmem_st32(tO + q4 * 32, ov);
+                        }
+                        tmem_wait_st();
+                    }
+                    const bool live = valid && m_run != -INFINITY;
+                    const float neg_m = -m_run;
+                    float la[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 1
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        uint32_t pa[32], pb[32];
+                        tmem_ld32(tS + h2 * 64, pa);
+                        tmem_ld32(tS + h2 * 64 + 32, pb);
+                        tmem_wait_ld();
+                        // P in place of the scores (as bit patterns): pa = columns 0..31, pb = 32..63
+                        if (live && full_tile) {
 #pragma unroll
                             for (int cc = 0; cc < 32; ++cc) {
-                                mxa[cc & 7] = fmaxf(mxa[cc & 7], __uint_as_float(pa[cc]));
-                                mxa[cc & 7] = fmaxf(mxa[cc & 7], __uint_as_float(pb[cc]));
+                                pa[cc] = __float_as_uint(ex2(fmaf(__uint_as_float(pa[cc]), sl2, neg_m)));
+                                pb[cc] = __float_as_uint(ex2(fmaf(__uint_as_float(pb[cc]), sl2, neg_m)));
                             }
-                        } else {
+                        } else if (live) {
 #pragma unroll
                             for (int cc = 0; cc < 32; ++cc) {
                                 const int c0 = h2 * 64 + cc;
-                                if (key_visible(t0 + c0, k_end, L, anc0, anc1, anc2, anc3))
-                                    mxa[cc & 7] = fmaxf(mxa[cc & 7], __uint_as_float(pa[cc]));
-                                if (key_visible(t0 + c0 + 32, k_end, L, anc0, anc1, anc2, anc3))
-                                    mxa[cc & 7] = fmaxf(mxa[cc & 7], __uint_as_float(pb[cc]));
+                                pa[cc] = key_visible(t0 + c0, k_end, L, anc0, anc1, anc2, anc3)
+                                             ? __float_as_uint(ex2(fmaf(__uint_as_float(pa[cc]), sl2, neg_m)))
+                                             : 0u;
+                                pb[cc] = key_visible(t0 + c0 + 32, k_end, L, anc0, anc1, anc2, anc3)
+                                             ? __float_as_uint(ex2(fmaf(__uint_as_float(pb[cc]), sl2, neg_m)))
+                                             : 0u;
                             }
-                        }
-                    }
-                }
-                const float mx_raw = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
-                                           fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
-                const float mx = mx_raw * sl2;  // scale > 0: max commutes with it
-                // the PV product of the previous tile must be done before O or P change
-                if (j > 0) {
-                    ok = __all_sync(0xffffffffu, mbar_wait(bar(Bars::kO + wg), (j - 1) & 1, s_abort));
-                    tc_fence_after();
-                }
-                const float m_new = fmaxf(m_run, mx);
-                bool rescale = false;
-                float factor = 1.0f;
-                if (m_run == -INFINITY) {
-                    m_run = m_new;
-                } else if (m_new > m_run + 8.0f) {
-                    factor = ex2(m_run - m_new);
-                    m_run = m_new;
-                    rescale = true;
-                }
-                l_run *= factor;
-                if (__any_sync(0xffffffffu, rescale) && ok) {
-#pragma unroll 1
-                    for (int q4 = 0; q4 < D / 32; ++q4) {
-                        uint32_t ov[32];
-                        tmem_ld32(tO + q4 * 32, ov);
-                        tmem_wait_ld();
+                        } else {
 #pragma unroll
-                        for (int cc = 0; cc < 32; ++cc) ov[cc] = __float_as_uint(__uint_as_float(ov[cc]) * factor);
-                        tmem_st32(tO + q4 * 32, ov);
+                            for (int cc = 0; cc < 32; ++cc) pa[cc] = pb[cc] = 0u;
+                        }
+                        // pack to bf16 pairs and store over the S columns already read
+                        uint32_t w[32];
+#pragma unroll
+                        for (int q = 0; q < 32; ++q) {
+                            const float p0 = __uint_as_float(q < 16 ? pa[2 * q] : pb[2 * q - 32]);
+                            const float p1 = __uint_as_float(q < 16 ? pa[2 * q + 1] : pb[2 * q - 31]);
+                            la[q & 3] += p0 + p1;
+                            __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
+                            w[q] = *reinterpret_cast<uint32_t*>(&pk);
+                        }
+                        tmem_st32(tS + h2 * 32, w);
                     }
                     tmem_wait_st();
+                    l_run += (la[0] + la[1]) + (la[2] + la[3]);
                 }
-                const bool live = valid && m_run != -INFINITY;
-                const float neg_m = -m_run;
-                float la[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                // a unit's last tile: V rows past the key range are zeroed before the PV
+                // product (they may hold stale or foreign data; P is 0 there but 0 * NaN is NaN)
+                if (wg == 0 && k_end - t0 < kTileKeys) {
+                    const int fV = 2 * jt + 1;
+                    ok = ok && mbar_wait(bar(Bars::kFull + fV % nslots), (fV / nslots) & 1, s_abort);
+                    if (ok) {
+                        uint8_t* vt = smem + lay.ring + (fV % nslots) * SLOT;
+                        const int row0 = k_end - t0;
+                        for (int idx = tw; idx < (kTileKeys - row0) * HALVES * 8; idx += 128) {
+                            const int per_half = (kTileKeys - row0) * 8;
+                            const int hh = idx / per_half, rem = idx % per_half;
+                            const int row = row0 + rem / 8, cq = rem % 8;
+                            *reinterpret_cast<uint4*>(vt + hh * kHalfBytes + row * 128 + cq * 16) = make_uint4(0, 0, 0, 0);
+                        }
+                    }
+                }
+                fence_proxy_async_smem();  // the zeroed V rows, written through the generic proxy
+                tc_fence_before();
+                mbar_arrive(bar(Bars::kP + sb));
+                if (!ok) *s_abort = 1;
+            }
+            // ---- next segment's Q: every S product of this segment has been read
+            TileIt nx = it;
+            if (jt < count) {
+                nx.next_unit(a);
+                load_q(nx.b, nx.g);
+            }
+            // ---- epilogue: O / l of this segment
+            if (ok) {
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(Bars::kO + wg), (jt - 1) & 1, s_abort));
+                tc_fence_after();
+                if (!ok) *s_abort = 1;
+            }
+            const int side = seg == 0 ? 0 : 1;  // a piece is this CTA's first or its last segment
+            if (ok && warp_active) {
+                const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;  // a piece may see no key of a row
+                const long long orow = (((long long)b * N + n) * a.Hq + g * a.G + hj) * D;
+                const long long prow = ((long long)blockIdx.x * 2 + side) * a.rows_item + wg * 128 + rl;
 #pragma unroll 1
-                for (int h2 = 0; h2 < 2; ++h2) {
-                    uint32_t pa[32], pb[32];
-                    tmem_ld32(tS + h2 * 64, pa);
-                    tmem_ld32(tS + h2 * 64 + 32, pb);
+                for (int q4 = 0; q4 < D / 32; ++q4) {
+                    uint32_t ov[32];
+                    tmem_ld32(tO + q4 * 32, ov);
                     tmem_wait_ld();
-                    // P in place of the scores (as bit patterns): pa = columns 0..31, pb = 32..63
-                    if (live && full_tile) {
+                    if (valid) {
+                        if (whole) {
+                            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow + q4 * 32);
 #pragma unroll
-                        for (int cc = 0; cc < 32; ++cc) {
-                            pa[cc] = __float_as_uint(ex2(fmaf(__uint_as_float(pa[cc]), sl2, neg_m)));
-                            pb[cc] = __float_as_uint(ex2(fmaf(__uint_as_float(pb[cc]), sl2, neg_m)));
-                        }
-                    } else if (live) {
+                            for (int v8 = 0; v8 < 4; ++v8) {
+                                uint32_t w[4];
 #pragma unroll
-                        for (int cc = 0; cc < 32; ++cc) {
-                            const int c0 = h2 * 64 + cc;
-                            pa[cc] = key_visible(t0 + c0, k_end, L, anc0, anc1, anc2, anc3)
-                                         ? __float_as_uint(ex2(fmaf(__uint_as_float(pa[cc]), sl2, neg_m)))
-                                         : 0u;
-                            pb[cc] = key_visible(t0 + c0 + 32, k_end, L, anc0, anc1, anc2, anc3)
-                                         ? __float_as_uint(ex2(fmaf(__uint_as_float(pb[cc]), sl2, neg_m)))
-                                         : 0u;
-                        }
-                    } else {
-#pragma unroll
-                        for (int cc = 0; cc < 32; ++cc) pa[cc] = pb[cc] = 0u;
-                    }
-                    // pack to bf16 pairs and store over the S columns already read
-                    uint32_t w[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float p0 = __uint_as_float(i < 16 ? pa[2 * i] : pb[2 * i - 32]);
-                        const float p1 = __uint_as_float(i < 16 ? pa[2 * i + 1] : pb[2 * i - 31]);
-                        la[i & 3] += p0 + p1;
-                        __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
-                        w[i] = *reinterpret_cast<uint32_t*>(&pk);
-                    }
-                    tmem_st32(tS + h2 * 32, w);
-                }
-                tmem_wait_st();
-                l_run += (la[0] + la[1]) + (la[2] + la[3]);
-            }
-            // the last tile's V rows past the key range are zeroed before the PV product
-            // (they may hold stale or foreign data; P is 0 there but 0 * NaN is NaN)
-            if (wg == 0 && j == ntiles - 1 && k_end - t0 < kTileKeys) {
-                const int fV = 2 * j + 1;
-                ok = ok && mbar_wait(bar(Bars::kFull + fV % nslots), (fV / nslots) & 1, s_abort);
-                if (ok) {
-                    uint8_t* vt = smem + lay.ring + (fV % nslots) * SLOT;
-                    const int row0 = k_end - t0;
-                    const int nbytes_row = 128;
-                    for (int idx = tw; idx < (kTileKeys - row0) * HALVES * (nbytes_row / 16); idx += 128) {
-                        const int per_half = (kTileKeys - row0) * 8;
-                        const int hh = idx / per_half, rem = idx % per_half;
-                        const int row = row0 + rem / 8, cq = rem % 8;
-                        *reinterpret_cast<uint4*>(vt + hh * kHalfBytes + row * 128 + cq * 16) = make_uint4(0, 0, 0, 0);
-                    }
-                }
-            }
-            fence_proxy_async_smem();  // the zeroed V rows, written through the generic proxy
-            tc_fence_before();
-            mbar_arrive(bar(Bars::kP + sb));
-            if (!ok) break;
-        }
-        // epilogue: O / l
-        if (ok && wg < nm && ntiles > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(bar(Bars::kO + wg), (ntiles - 1) & 1, s_abort));
-            tc_fence_after();
-        }
-        if (ok && warp_active) {
-            const float inv = 1.0f / l_run;
-            const long long orow = (((long long)b * N + n) * a.Hq + h) * D;
-            const long long prow = (((long long)b * a.Hkv + g) * a.max_chunks + c) * a.R + r;
-#pragma unroll
-            for (int q4 = 0; q4 < D / 32; ++q4) {
-                uint32_t ov[32];
-                tmem_ld32(tO + q4 * 32, ov);
-                tmem_wait_ld();
-                if (valid) {
-                    if (nch == 1) {
-                        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow + q4 * 32);
-#pragma unroll
-                        for (int v8 = 0; v8 < 4; ++v8) {
-                            uint32_t w[4];
-#pragma unroll
-                            for (int e2 = 0; e2 < 4; ++e2) {
-                                __nv_bfloat162 pk = __floats2bfloat162_rn(__uint_as_float(ov[v8 * 8 + 2 * e2]) * inv,
-                                                                          __uint_as_float(ov[v8 * 8 + 2 * e2 + 1]) * inv);
-                                w[e2] = *reinterpret_cast<uint32_t*>(&pk);
+                                for (int e2 = 0; e2 < 4; ++e2) {
+                                    __nv_bfloat162 pk =
+                                        __floats2bfloat162_rn(__uint_as_float(ov[v8 * 8 + 2 * e2]) * inv,
+                                                              __uint_as_float(ov[v8 * 8 + 2 * e2 + 1]) * inv);
+                                    w[e2] = *reinterpret_cast<uint32_t*>(&pk);
+                                }
+                                dst[v8] = make_uint4(w[0], w[1], w[2], w[3]);
                             }
-                            dst[v8] = make_uint4(w[0], w[1], w[2], w[3]);
-                        }
-                    } else {
-                        float4* dst = reinterpret_cast<float4*>(a.part_o + prow * D + q4 * 32);
+                        } else {
+                            float4* dst = reinterpret_cast<float4*>(a.part_o + prow * D + q4 * 32);
 #pragma unroll
-                        for (int v4 = 0; v4 < 8; ++v4)
-                            dst[v4] = make_float4(__uint_as_float(ov[v4 * 4]) * inv, __uint_as_float(ov[v4 * 4 + 1]) * inv,
-                                                  __uint_as_float(ov[v4 * 4 + 2]) * inv,
-                                                  __uint_as_float(ov[v4 * 4 + 3]) * inv);
+                            for (int v4 = 0; v4 < 8; ++v4)
+                                dst[v4] = make_float4(__uint_as_float(ov[v4 * 4]) * inv, __uint_as_float(ov[v4 * 4 + 1]) * inv,
+                                                      __uint_as_float(ov[v4 * 4 + 2]) * inv,
+                                                      __uint_as_float(ov[v4 * 4 + 3]) * inv);
+                        }
                     }
                 }
+                if (valid && !whole) {
+                    a.part_m[prow] = m_run;
+                    a.part_l[prow] = l_run;
+                }
             }
-            if (valid && nch > 1) {
-                a.part_m[prow] = m_run;
-                a.part_l[prow] = l_run;
-            }
+            it = nx;
+            ++seg;
         }
         if (!ok) my_err = 1;
     }
     if (my_err) {
         *s_abort = 1;
-        atomicOr(&a.seq_err[b], TSV_DERR_TIMEOUT);
+        atomicOr(&a.seq_err[err_b], TSV_DERR_TIMEOUT);
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+// Merge of the units that straddle lanes (log-sum-exp over their pieces).  One CTA per
+// (unit, block of 32 rows); 8 threads per row, each owning D / 8 consecutive columns,
+// so a row's 8 threads read its partial rows as one coalesced run.  Runs after the
+// attention kernel (programmatic dependent launch: it waits for that kernel's writes).
+template <int D>
+__global__ void __launch_bounds__(256) attn_tc_merge_kernel(const AttnArgs a) {
+    constexpr int C = D / 8;  // columns per thread
+    pdl_wait();
+    const int nrg = a.n_rgroups;
+    const int u = blockIdx.x;
+    const int rg = u % nrg, g = (u / nrg) % a.Hkv, b = u / (nrg * a.Hkv);
+    const int* ui = a.unit_info + (long long)u * kUnitInfoInts;
+    const int e = a.seq_err[b];
+    const int c_first = ui[0], c_last = ui[1], sd0 = ui[2];
+    const long long T_all = reinterpret_cast<const long long*>(ui)[2];
+    if (e != 0) return;  // flagged (NaN rows) or timed out
+    if (c_last <= c_first || c_first < 0 || c_last >= a.lanes || T_all < 1) return;  // one piece: written directly
+    const int r_base = rg * 256;
+    const int rows_rg = min(256, a.R - r_base);
+    const int rr = blockIdx.y * 32 + (threadIdx.x >> 3), c0 = (threadIdx.x & 7) * C;
+    if (rr >= rows_rg) return;
+    const bool dense = T_all >= a.lanes;  // every lane has a non-empty run
+    float acc[C];
+#pragma unroll
+    for (int q = 0; q < C; ++q) acc[q] = 0.0f;
+    float M = -INFINITY, W = 0.0f;
+    if (dense && c_last - c_first < 4) {
+        // up to four pieces: every load is issued before any is used
+        constexpr int P = 4;
+        float lk[P], mk[P];
+        float4 o[P][C / 4];
+#pragma unroll
+        for (int k = 0; k < P; ++k) {
+            lk[k] = 0.0f;
+            mk[k] = -INFINITY;
+            if (c_first + k <= c_last) {
+                const long long pr = ((long long)((c_first + k) * nrg + rg) * 2 + (k == 0 ? sd0 : 0)) * a.rows_item + rr;
+                lk[k] = __ldg(a.part_l + pr);
+                mk[k] = __ldg(a.part_m + pr);
+                const float4* src = reinterpret_cast<const float4*>(a.part_o + pr * D + c0);
+#pragma unroll
+                for (int q = 0; q < C / 4; ++q) o[k][q] = __ldg(src + q);
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < P; ++k)
+            if (lk[k] > 0.0f) M = fmaxf(M, mk[k]);
+#pragma unroll
+        for (int k = 0; k < P; ++k) {
+            const float wk = lk[k] > 0.0f ? lk[k] * exp2f(mk[k] - M) : 0.0f;  // a piece may see no key of a row
+            W += wk;
+            if (wk > 0.0f) {
+#pragma unroll
+                for (int q = 0; q < C / 4; ++q) {
+                    acc[4 * q] = fmaf(wk, o[k][q].x, acc[4 * q]);
+                    acc[4 * q + 1] = fmaf(wk, o[k][q].y, acc[4 * q + 1]);
+                    acc[4 * q + 2] = fmaf(wk, o[k][q].z, acc[4 * q + 2]);
+                    acc[4 * q + 3] = fmaf(wk, o[k][q].w, acc[4 * q + 3]);
+                }
+            }
+        }
+    } else {
+        for (int k = c_first; k <= c_last; ++k) {
+            if (!dense && lane_start(k + 1, T_all, a.lanes) == lane_start(k, T_all, a.lanes)) continue;
+            const long long pr = ((long long)(k * nrg + rg) * 2 + (k == c_first ? sd0 : 0)) * a.rows_item + rr;
+            const float lk = __ldg(a.part_l + pr), mk = __ldg(a.part_m + pr);
+            if (!(lk > 0.0f)) continue;
+            if (mk > M) {
+                W = W * exp2f(M - mk) + lk;
+                M = mk;
+            } else {
+                W += lk * exp2f(mk - M);
+            }
+        }
+        for (int k = c_first; k <= c_last; ++k) {
+            if (!dense && lane_start(k + 1, T_all, a.lanes) == lane_start(k, T_all, a.lanes)) continue;
+            const long long pr = ((long long)(k * nrg + rg) * 2 + (k == c_first ? sd0 : 0)) * a.rows_item + rr;
+            const float lk = __ldg(a.part_l + pr);
+            if (!(lk > 0.0f)) continue;
+            const float wk = lk * exp2f(__ldg(a.part_m + pr) - M);
+            const float4* src = reinterpret_cast<const float4*>(a.part_o + pr * D + c0);
+#pragma unroll
+            for (int q = 0; q < C / 4; ++q) {
+                const float4 o = __ldg(src + q);
+                acc[4 * q] = fmaf(wk, o.x, acc[4 * q]);
+                acc[4 * q + 1] = fmaf(wk, o.y, acc[4 * q + 1]);
+                acc[4 * q + 2] = fmaf(wk, o.z, acc[4 * q + 2]);
+                acc[4 * q + 3] = fmaf(wk, o.w, acc[4 * q + 3]);
+            }
+        }
+    }
+    const float winv = 1.0f / W;
+    const int r = r_base + rr;
+    uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) +
+                                          (((long long)b * a.N + r / a.G) * a.Hq + g * a.G + r % a.G) * D + c0);
+#pragma unroll
+    for (int q = 0; q < C / 8; ++q) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            __nv_bfloat162 pk = __floats2bfloat162_rn(acc[8 * q + 2 * e] * winv, acc[8 * q + 2 * e + 1] * winv);
+            w[e] = *reinterpret_cast<uint32_t*>(&pk);
+        }
+        dst[q] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+// launches `kernel` with programmatic stream serialisation: it may start while the
+// previous kernel in the stream finishes, and waits for it with griddepcontrol.wait
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
@@ -752,22 +1060,57 @@ bool make_cache_map(CUtensorMap* map, const void* base, int D, int Hkv, long lon
     return r == CUDA_SUCCESS;
 }
 
+// The tensor maps of the most recent caches this host thread used (encoding them costs
+// microseconds of host time per call).
+struct MapCache {
+    const void* k = nullptr;
+    const void* v = nullptr;
+    int D = 0, Hkv = 0, bs = 0;
+    long long rows = 0;
+    CUtensorMap mk, mv;
+};
+
 template <int D>
 cudaError_t launch_tc_inst(const AttnArgs& a, cudaStream_t stream) {
-    CUtensorMap mk, mv;
+    thread_local MapCache mc;
     const long long rows = static_cast<long long>(a.num_blocks) << a.bs_log2;
-    if (!make_cache_map(&mk, a.k_cache, D, a.Hkv, rows, 1 << a.bs_log2) ||
-        !make_cache_map(&mv, a.v_cache, D, a.Hkv, rows, 1 << a.bs_log2))
-        return cudaErrorInvalidValue;
+    const int bs = 1 << a.bs_log2;
+    if (mc.k != a.k_cache || mc.v != a.v_cache || mc.D != D || mc.Hkv != a.Hkv || mc.bs != bs || mc.rows != rows) {
+        mc.k = nullptr;
+        if (!make_cache_map(&mc.mk, a.k_cache, D, a.Hkv, rows, bs) || !make_cache_map(&mc.mv, a.v_cache, D, a.Hkv, rows, bs))
+            return cudaErrorInvalidValue;
+        mc.k = a.k_cache;
+        mc.v = a.v_cache;
+        mc.D = D;
+        mc.Hkv = a.Hkv;
+        mc.bs = bs;
+        mc.rows = rows;
+    }
+    const CUtensorMap& mk = mc.mk;
+    const CUtensorMap& mv = mc.mv;
+    attn_tc_check_kernel<<<static_cast<unsigned>(a.B), 128, 0, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
     const int nm_max = a.R > 128 ? 2 : 1;
     const TcLayout lay = tc_layout<D>(nm_max);
-    cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(lay.total));
+    // the kernel's dynamic shared memory limit, raised once per device and host thread
+    thread_local int smem_dev = -1, smem_set = -1;
+    int dev = 0;
+    e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    dim3 grid(static_cast<unsigned>(a.n_rgroups * a.max_chunks), static_cast<unsigned>(a.Hkv),
-              static_cast<unsigned>(a.B));
-    attn_tc_kernel<D><<<grid, kThreads, lay.total, stream>>>(a, mk, mv, nm_max);
-    return cudaGetLastError();
+    if (dev != smem_dev || static_cast<int>(lay.total) > smem_set) {
+        e = cudaFuncSetAttribute(attn_tc_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(lay.total));
+        if (e != cudaSuccess) return e;
+        smem_dev = dev;
+        smem_set = static_cast<int>(lay.total);
+    }
+    e = launch_pdl(attn_tc_kernel<D>, dim3(static_cast<unsigned>(a.lanes * a.n_rgroups)), dim3(kThreads), lay.total,
+                   stream, a, mk, mv, nm_max);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(attn_tc_merge_kernel<D>,
+                      dim3(static_cast<unsigned>(a.B * a.Hkv * a.n_rgroups), static_cast<unsigned>((a.rows_item + 31) / 32)),
+                      dim3(256), 0, stream, a);
 }
 
 }  // namespace
