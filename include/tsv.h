@@ -154,9 +154,11 @@ tsv_status tsv_tree_verify_attn_noalloc(const void *q, const void *k_cache, cons
  * drafts accepted (path length - 1); bonus_token[b]; out_tokens[b,:] = accepted
  * draft tokens then the bonus, -1 padded.  A sequence with seq_err != 0 gets
  * accept_len = bonus_token = -1 and all-(-1) rows.
- * Uniforms are pre-drawn by the caller in [0, 1).  Vocabulary-wide sums use fp32
- * per thread and fp64 across threads; the ratio p(x)/q(x) itself is evaluated in
- * fp64.  V <= 16 * 1024 * 32.
+ * Uniforms are pre-drawn by the caller in [0, 1).  T == 0 or T >= 1e-6 (smaller
+ * positive T is refused with TSV_ERR_UNSUPPORTED).  Vocabulary-wide sums use fp32
+ * per thread and float-float pairs (about 44 significant bits) across threads, warps
+ * and CTAs; the ratio p(x)/q(x) is formed in float-float from a compensated exponent
+ * argument (relative error a few 1e-7).  V <= 16 * 512 * 32.
  * ------------------------------------------------------------------------- */
 tsv_status tsv_tree_reject_sample(const float *target_logits, const float *draft_probs,
                                   const int32_t *draft_tokens, const int32_t *parent,

@@ -173,6 +173,8 @@ tsv_status tsv_tree_reject_sample(const float* target_logits, const float* draft
     if (N > tsv::kMaxNodes) return fail(TSV_ERR_UNSUPPORTED, "N=%d exceeds %d tree nodes", N, tsv::kMaxNodes);
     if (V > 16 * 512 * 32) return fail(TSV_ERR_UNSUPPORTED, "V=%d exceeds %d", V, 16 * 512 * 32);
     if (!(temperature >= 0.0f) || !isfinite(temperature)) return fail(TSV_ERR_ARG, "temperature must be finite and >= 0");
+    if (temperature > 0.0f && temperature < 1e-6f)
+        return fail(TSV_ERR_UNSUPPORTED, "temperature %g in (0, 1e-6): use 0 for greedy matching", temperature);
     if (B == 0) return TSV_OK;
     const bool greedy = temperature == 0.0f;
     if (!target_logits || !draft_tokens || !parent || !accepted_nodes || !accept_len || !bonus_token ||

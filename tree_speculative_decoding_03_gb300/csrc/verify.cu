@@ -25,6 +25,15 @@
 // two-sum/two-product transformations, about 44 significant bits), and the
 // acceptance ratio p(x)/q(x) is formed in float-float from a compensated exponent
 // argument; its error is dominated by expf's (<= 2 ulp), a few 1e-7 relative.
+// Vocabulary-wide passes take each entry as 2^(l c - MC) with c = log2(e) / T and
+// MC = fl(M c) (one FMA and one ex2.approx, ~2 ulp): the same offset for every entry
+// keeps the pass's p self-normalised, and the normaliser handed to the ratio is
+// corrected by the exactly computed rounding of M c.
+//
+// The children of the current node are tested in parallel lanes: each keeps its
+// (p(x), q(x)) at the current residual level in shared memory, updated once per
+// rejection, so a test is a comparison and a rejection costs one pass and one
+// cluster reduction whatever the number of earlier rejections.
 #include <cooperative_groups.h>
 
 #include <map>
@@ -66,6 +75,12 @@ __device__ __forceinline__ ff ff_mul_f(ff a, float b) {
     const float p = a.hi * b;
     float e = fmaf(a.hi, b, -p);
     e = fmaf(a.lo, b, e);
+    return quick_two_sum(p, e);
+}
+__device__ __forceinline__ ff ff_mul(ff a, ff b) {
+    const float p = a.hi * b.hi;
+    float e = fmaf(a.hi, b.hi, -p);
+    e = fmaf(a.hi, b.lo, fmaf(a.lo, b.hi, e));
     return quick_two_sum(p, e);
 }
 __device__ __forceinline__ ff ff_div(ff a, ff b) {
@@ -117,12 +132,18 @@ __device__ __forceinline__ void warp_argmax(float& v, int& i) {
     }
 }
 
-// x / T from a precomputed 1/T with one Newton correction (within an ulp of the
-// correctly rounded quotient; exact for T == 1) -- a full IEEE division per element
-// costs far more than the two FMAs
-__device__ __forceinline__ float div_t(float x, float T, float invT) {
-    const float q = x * invT;
-    return isfinite(q) ? fmaf(fmaf(-q, T, x), invT, q) : q;  // -inf (padding) stays -inf
+// ----------------------------------------------------------------------------- async copies
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+// one 4-byte global -> shared copy that completes asynchronously (cp.async.wait_group)
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // true iff v is one of the first j rejected tokens xr[0..j-1]
@@ -217,17 +238,21 @@ enum { kRedStats = 0, kRedSums = 1, kRedArgmax = 2 };
 
 // Cluster all-reduce: every CTA publishes `mine` in its own slot[parity], the
 // cluster synchronises, and warp 0 of every CTA combines all slots in rank order
-// (so every CTA obtains bit-identical results).  Stats: (max a, sum hi+lo of
-// exp((x - a)/T)) with per-slot rescaling; sums: two float-float sums; argmax:
+// (so every CTA obtains bit-identical results).  Stats: (raw max a, sum hi+lo of
+// 2^(x c - fl(a c))) with per-slot rescaling; sums: two float-float sums; argmax:
 // (a, i).  Must be called by every thread of every CTA; the result is in *res
 // after the closing __syncthreads.  Slots alternate by parity, so the write of the
 // next reduction cannot overtake a slow CTA still reading this one.
 __device__ __forceinline__ void cluster_allreduce(cg::cluster_group& cluster, RedSlot* slots, int parity,
-                                                  const RedSlot& mine, int kind, float T, RedSlot* res) {
+                                                  const RedSlot& mine, int kind, float c2, RedSlot* res,
+                                                  bool wait_async = false) {
     const int tid = threadIdx.x, lane = tid & 31;
     const int cs = (int)cluster.num_blocks();
     if (tid == 0) slots[parity] = mine;
     cluster.sync();
+    // the last warp's asynchronous copies land while the cluster combines; the closing
+    // barrier makes them visible to the whole CTA
+    if (wait_async && (tid >> 5) == (int)(blockDim.x >> 5) - 1) asm volatile("cp.async.wait_all;" ::: "memory");
     if (tid < 32) {
         RedSlot r{};
         r.a = -INFINITY;
@@ -239,7 +264,7 @@ __device__ __forceinline__ void cluster_allreduce(cg::cluster_group& cluster, Re
         if (kind == kRedStats) {
             const float m = warp_max(lane < cs ? r.a : -INFINITY);
             ff c = ff_make(0.0f);
-            if (lane < cs && (r.hi > 0.0f)) c = ff_mul_f(ff{r.hi, r.lo}, expf((r.a - m) / T));
+            if (lane < cs && (r.hi > 0.0f)) c = ff_mul_f(ff{r.hi, r.lo}, exp2f(r.a * c2 - m * c2));
             c = warp_sum_ff(c);
             o.a = m;
             o.hi = c.hi;
@@ -270,7 +295,7 @@ __device__ __forceinline__ void cluster_allreduce(cg::cluster_group& cluster, Re
 // residual sum is exactly zero).
 template <int VEC, bool ALIGNED>
 __device__ __forceinline__ void rebuild_level(float (&lv)[VEC][4], const float* lrow, const float* qrow, int v0, int v1,
-                                           int level, float M, float T, float invT, float invZ, const int* xrej,
+                                           int level, float c2, float MC, float invZ, const int* xrej,
                                            const float* inv_sq, const float* inv_zr, const int* zr_ok) {
     load_slice<VEC, ALIGNED>(lrow, v0, v1, lv, -INFINITY);
 #pragma unroll
@@ -281,7 +306,7 @@ __device__ __forceinline__ void rebuild_level(float (&lv)[VEC][4], const float* 
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int v = base + e;
-            float p = expf(div_t(lv[k][e] - M, T, invT)) * invZ;
+            float p = ex2(fmaf(lv[k][e], c2, -MC)) * invZ;
             for (int j = 1; j <= level; ++j) {
                 const float qprev = (j == 1) ? qk[e] : (is_rejected(v, j - 1, xrej) ? 0.0f : qk[e] * inv_sq[j - 1]);
                 if (zr_ok[j]) p = fmaxf(0.0f, p - qprev) * inv_zr[j];
@@ -302,21 +327,23 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
     const int v0 = min(V, rank * a.v_per_cta), v1 = min(V, v0 + a.v_per_cta);
     const bool greedy = (a.T == 0.0f);
     const float T = a.T;
-    const float invT = greedy ? 0.0f : 1.0f / a.T;
+    const float c2 = greedy ? 0.0f : 1.4426950408889634f / a.T;  // log2(e) / T
 
     __shared__ int s_par[kMaxNodes], s_tok[kMaxNodes], s_path[kMaxNodes];
     __shared__ int s_kids[kMaxNodes];
     __shared__ float s_lx[kMaxNodes], s_qx[kMaxNodes], s_ux[kMaxNodes];
+    // per child of the current node: p(x), q(x) at the current residual level, and
+    // whether its token has already been rejected at this node
+    __shared__ ff s_px[kMaxNodes], s_qc[kMaxNodes];
+    __shared__ int s_rflag[kMaxNodes];
     __shared__ RedSlot s_red[2];
     __shared__ RedSlot s_cta;  // this CTA's partial
     __shared__ RedSlot s_all;  // cluster result
     __shared__ float s_wf[32], s_wg[32];
     __shared__ int s_wi[32], s_wb[32];
-    __shared__ int s_nk, s_flag, s_accept, s_err2;
-    __shared__ float s_invz;
+    __shared__ int s_nk, s_flag;
     // rejection history at the current node
     __shared__ int s_xrej[kMaxRejections];        // rejected tokens x_1..x_j
-    __shared__ float s_qrej[kMaxRejections];      // their raw draft probabilities
     __shared__ ff s_zr[kMaxRejections + 1];       // residual sums Zr_j (level j >= 1)
     __shared__ ff s_sq[kMaxRejections + 1];       // S_j = sum of q over tokens not in {x_1..x_j}
     __shared__ float s_inv_zr[kMaxRejections + 1], s_inv_sq[kMaxRejections + 1];
@@ -325,6 +352,12 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
     __shared__ ff s_segcum[8 * 16];  // bonus: inclusive prefix over (k, warp)
     __shared__ ff s_target;
     __shared__ int s_claim, s_segsel;
+    // aligned rows: the first rejection pass at a node keeps this CTA's slice of the
+    // node's draft row in shared memory for the node's later passes
+    extern __shared__ float4 s_dyn[];
+    float* s_q = reinterpret_cast<float*>(s_dyn);
+    const bool bulk = ALIGNED && v1 > v0;
+    const ff invT_ff = greedy ? ff_make(0.0f) : ff_div(ff_make(1.0f), ff_make(T));
 
     int parity = 0;
 
@@ -347,8 +380,9 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
     // residual r instead of the logits; the current p is r * pscale.
     bool lv_is_p = false;
     float pscale = 0.0f;
-    float M = 0.0f;
-    ff Z = ff_make(1.0f), Qsum = ff_make(0.0f);
+    float M = 0.0f, MC = 0.0f;  // raw max logit of the row, fl(M c2)
+    float invZf = 1.0f;         // 1 / sum of 2^(l c2 - MC): the passes' normaliser
+    ff Qsum = ff_make(0.0f);
     int amax = 0;
 
     while (!err) {
@@ -368,24 +402,25 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
         }
         __syncthreads();
         const int nk = s_nk;
-        // the last warp fetches the scalars the children's tests need; the rest of the
-        // block starts on the row
+        // the last warp starts asynchronous copies of the scalars the children's tests
+        // need (they land while the row is reduced); the rest of the block starts on the row
         if (warp == nwarps - 1) {
             for (int t = lane; t < nk; t += 32) {
                 const int x = s_tok[s_kids[t]];
+                s_qx[t] = 0.0f;
                 if (x >= 0 && x < V) {
-                    s_lx[t] = __ldg(lrow + x);
+                    cp_async4(&s_lx[t], lrow + x);
                     if (!greedy) {
-                        s_qx[t] = __ldg(qrow + x);
-                        s_ux[t] = __ldg(a.u_accept + (long long)b * N + s_kids[t]);
+                        cp_async4(&s_qx[t], qrow + x);
+                        cp_async4(&s_ux[t], a.u_accept + (long long)b * N + s_kids[t]);
                     }
                 }
             }
+            cp_async_commit();
         }
         load_slice<VEC, ALIGNED>(lrow, v0, v1, lv, -INFINITY);
-        // likely next rows into L2: the first child's logits row and this node's draft row
+        // the first child's logits row into L2, for the likely case that it is accepted
         if (nk > 0) prefetch_slice<VEC>(a.logits + ((long long)b * N + s_kids[0]) * V, v0, v1);
-        if (!greedy && nk > 0) prefetch_slice<VEC>(qrow, v0, v1);
 
         int bad = 0;
 #pragma unroll
@@ -431,11 +466,11 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                 }
             }
             __syncthreads();
-            cluster_allreduce(cluster, s_red, parity, s_cta, kRedArgmax, T, &s_all);
+            cluster_allreduce(cluster, s_red, parity, s_cta, kRedArgmax, c2, &s_all, true);
             parity ^= 1;
             amax = s_all.i;
         } else {
-            // per warp: max m_w and sum of exp((l - m_w)/T) in fp32
+            // per warp: raw max m_w and sum of 2^(l c2 - fl(m_w c2)), fp32, 4 accumulators
             float m = -INFINITY;
 #pragma unroll
             for (int k = 0; k < VEC; ++k)
@@ -444,11 +479,12 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
             m = warp_max(m);
             float sacc = 0.0f;
             if (m > -INFINITY) {
+                const float mc = m * c2;
                 float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
                 for (int k = 0; k < VEC; ++k)
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) s4[e] += expf(div_t(lv[k][e] - m, T, invT));
+                    for (int e = 0; e < 4; ++e) s4[e] += ex2(fmaf(lv[k][e], c2, -mc));  // padding: 2^-inf = 0
                 sacc = (s4[0] + s4[1]) + (s4[2] + s4[3]);
             }
             sacc = warp_sum(sacc);
@@ -464,7 +500,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                 const float ws = lane < nwarps ? s_wg[lane] : 0.0f;
                 const int f = warp_or(lane < nwarps ? s_wb[lane] : 0);
                 const float cm = warp_max(wm);
-                ff c = ws > 0.0f ? ff_mul_f(ff_make(ws), expf((wm - cm) / T)) : ff_make(0.0f);
+                ff c = ws > 0.0f ? ff_mul_f(ff_make(ws), exp2f(wm * c2 - cm * c2)) : ff_make(0.0f);
                 c = warp_sum_ff(c);
                 if (lane == 0) {
                     RedSlot r{};
@@ -476,16 +512,37 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                 }
             }
             __syncthreads();
-            cluster_allreduce(cluster, s_red, parity, s_cta, kRedStats, T, &s_all);
+            cluster_allreduce(cluster, s_red, parity, s_cta, kRedStats, c2, &s_all, true);
             parity ^= 1;
             M = s_all.a;
-            Z = ff{s_all.hi, s_all.lo};
-            if (tid == 0) s_invz = ff_float(ff_div(ff_make(1.0f), Z));
+            MC = M * c2;
+            const ff Zf{s_all.hi, s_all.lo};
+            invZf = 1.0f / ff_float(Zf);
+            // the ratio's normaliser: sum of exp((l - M) / T), i.e. Zf without the rounding of M c2
+            const ff Z = ff_mul_f(Zf, exp2f(-fmaf(M, c2, -MC)));
+            const ff invZ = ff_div(ff_make(1.0f), Z);
+            // children's p(x), q(x) at level 0, one lane per child (p(x) in float-float from
+            // a compensated exponent argument)
+            if (warp == 0) {
+                for (int t = lane; t < nk; t += 32) {
+                    const float qraw = s_qx[t];
+                    ff px = ff_make(0.0f);
+                    if (isfinite(qraw)) {
+                        const ff arg = ff_mul(two_sum(s_lx[t], -M), invT_ff);
+                        const float ex = expf(arg.hi);
+                        px = ff_mul(quick_two_sum(ex, ex * arg.lo), invZ);
+                    }
+                    s_px[t] = px;
+                    s_qc[t] = ff_make(qraw);
+                    s_rflag[t] = 0;
+                }
+            }
         }
         if (s_all.flag) {
             err = TSV_DERR_NONFINITE;
             break;
         }
+        __syncthreads();
 
         // ---- children, in index order
         nrej = 0;
@@ -506,49 +563,19 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                 }
                 continue;
             }
-            // p(x)/q(x) at the current level, in float-float (thread 0; broadcast)
-            if (tid == 0) {
-                const float qraw = s_qx[t];
-                int e2 = 0, acc = 0;
-                if (!isfinite(qraw)) {
-                    e2 = TSV_DERR_NONFINITE;
-                } else {
-                    // p_0(x) = exp((l_x - M) / T) / Z with a compensated exponent argument
-                    const ff arg = ff_div(two_sum(s_lx[t], -M), ff_make(T));
-                    const float ex = expf(arg.hi);
-                    ff px = ff_div(quick_two_sum(ex, ex * arg.lo), Z);
-                    ff qx = ff_make(qraw);  // level 0: the raw draft probability
-                    bool x_rejected = false;
-                    for (int j = 1; j <= nrej; ++j) {
-                        // level j-1 -> j: residual on p, x_j removed from q
-                        if (s_zr_ok[j]) px = ff_div(ff_max0(ff_sub(px, qx)), s_zr[j]);
-                        if (s_xrej[j - 1] == x) x_rejected = true;
-                        qx = (x_rejected || !ff_pos(s_sq[j])) ? ff_make(0.0f) : ff_div(ff_make(qraw), s_sq[j]);
-                    }
-                    // u < p/q, i.e. u * q < p (q > 0); q == 0 accepts iff p > 0
-                    const float u = s_ux[t];
-                    if (ff_pos(qx))
-                        acc = ff_lt(ff_mul_f(qx, u), px) ? 1 : 0;
-                    else
-                        acc = ff_pos(px) ? 1 : 0;
-                }
-                s_err2 = e2;
-                s_accept = acc;
-            }
-            __syncthreads();
-            const int e2 = s_err2, accept = s_accept;
-            __syncthreads();
-            if (e2) {
-                err = e2;
+            if (!isfinite(s_qx[t])) {
+                err = TSV_DERR_NONFINITE;
                 break;
             }
+            // u < p/q, i.e. u * q < p (q > 0); q == 0 accepts iff p > 0
+            const ff px = s_px[t], qx = s_qc[t];
+            const bool accept = ff_pos(qx) ? ff_lt(ff_mul_f(qx, s_ux[t]), px) : ff_pos(px);
             if (accept) {
                 next = c;
                 break;
             }
             // rejected: residual sum at the next level (and, the first time, sum q)
             int qb = 0;
-            const float invZ = s_invz;
             const uint32_t excl = owned_mask<VEC>(s_xrej, nrej, v0, v1);  // tokens out of q at this level
             const float inv_sq = nrej > 0 ? s_inv_sq[nrej] : 1.0f;
             float zr = 0.0f, qs = 0.0f;
@@ -557,8 +584,21 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
             for (int k0 = 0; k0 < VEC; k0 += QG) {
                 float qk[QG][4];
 #pragma unroll
-                for (int kk = 0; kk < QG; ++kk)
-                    load4<ALIGNED>(qrow, v0 + ((k0 + kk) * (int)blockDim.x + tid) * 4, v1, qk[kk], 0.0f);
+                for (int kk = 0; kk < QG; ++kk) {
+                    const int off = ((k0 + kk) * (int)blockDim.x + tid) * 4;
+                    if (bulk && nrej > 0) {  // kept by this node's first pass
+                        float4 t = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                        if (v0 + off < v1) t = *reinterpret_cast<const float4*>(s_q + off);
+                        qk[kk][0] = t.x;
+                        qk[kk][1] = t.y;
+                        qk[kk][2] = t.z;
+                        qk[kk][3] = t.w;
+                    } else {
+                        load4<ALIGNED>(qrow, v0 + off, v1, qk[kk], 0.0f);
+                        if (bulk && v0 + off < v1)
+                            *reinterpret_cast<float4*>(s_q + off) = make_float4(qk[kk][0], qk[kk][1], qk[kk][2], qk[kk][3]);
+                    }
+                }
 #pragma unroll
                 for (int kk = 0; kk < QG; ++kk) {
                     const int k = k0 + kk;
@@ -569,7 +609,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                         const float q = qk[kk][e];
                         if (v < v1 && !isfinite(q)) qb = 1;
                         // p and q at the current level
-                        const float p = lv_is_p ? lv[k][e] * pscale : expf(div_t(lv[k][e] - M, T, invT)) * invZ;
+                        const float p = lv_is_p ? lv[k][e] * pscale : ex2(fmaf(lv[k][e], c2, -MC)) * invZf;
                         const float qc = (nrej == 0) ? q : (((excl >> (k * 4 + e)) & 1u) ? 0.0f : q * inv_sq);
                         const float d = fmaxf(0.0f, p - qc);
                         zr += d;
@@ -602,7 +642,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                 }
             }
             __syncthreads();
-            cluster_allreduce(cluster, s_red, parity, s_cta, kRedSums, T, &s_all);
+            cluster_allreduce(cluster, s_red, parity, s_cta, kRedSums, c2, &s_all);
             parity ^= 1;
             if (s_all.flag) {
                 err = TSV_DERR_NONFINITE;
@@ -610,24 +650,37 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
             }
             if (!q_loaded) Qsum = ff{s_all.hi2, s_all.lo2};
             q_loaded = true;
-            // record level nrej + 1
+            // level j = nrej + 1: its residual sum Zr_j and S_j = sum of q without the
+            // distinct rejected tokens; then every later child's (p, q) moves to level j
+            const int j = nrej + 1;
             const ff zr_new{s_all.hi, s_all.lo};
-            __syncthreads();
-            if (tid == 0) {
-                const int j = nrej + 1;
-                s_xrej[j - 1] = x;
-                s_qrej[j - 1] = s_qx[t];
-                s_zr[j] = zr_new;
-                s_zr_ok[j] = ff_pos(zr_new);
-                s_inv_zr[j] = ff_pos(zr_new) ? ff_float(ff_div(ff_make(1.0f), zr_new)) : 1.0f;
-                ff sq = Qsum;
-                for (int i2 = 0; i2 < j; ++i2) {  // subtract each distinct rejected token once
-                    bool dup = false;
-                    for (int i3 = 0; i3 < i2; ++i3) dup |= (s_xrej[i3] == s_xrej[i2]);
-                    if (!dup) sq = ff_sub(sq, ff_make(s_qrej[i2]));
+            if (warp == 0) {
+                bool dup = false;
+                for (int i2 = lane; i2 < nrej; i2 += 32) dup |= (s_xrej[i2] == x);
+                dup = __any_sync(0xffffffffu, dup);
+                const ff sq = dup ? (j == 1 ? Qsum : s_sq[j - 1]) : ff_sub(j == 1 ? Qsum : s_sq[j - 1], ff_make(s_qx[t]));
+                const bool zr_ok = ff_pos(zr_new);
+                __syncwarp();
+                if (lane == 0) {
+                    s_xrej[j - 1] = x;
+                    s_zr[j] = zr_new;
+                    s_zr_ok[j] = zr_ok;
+                    s_inv_zr[j] = zr_ok ? ff_float(ff_div(ff_make(1.0f), zr_new)) : 1.0f;
+                    s_sq[j] = sq;
+                    s_inv_sq[j] = ff_pos(sq) ? ff_float(ff_div(ff_make(1.0f), sq)) : 0.0f;
                 }
-                s_sq[j] = sq;
-                s_inv_sq[j] = ff_pos(sq) ? ff_float(ff_div(ff_make(1.0f), sq)) : 0.0f;
+                const ff inv_zr = zr_ok ? ff_div(ff_make(1.0f), zr_new) : ff_make(1.0f);
+                const ff inv_sq = ff_pos(sq) ? ff_div(ff_make(1.0f), sq) : ff_make(0.0f);
+                for (int t2 = t + 1 + lane; t2 < nk; t2 += 32) {
+                    ff p2 = s_px[t2];
+                    const ff q2 = s_qc[t2];
+                    if (zr_ok) p2 = ff_mul(ff_max0(ff_sub(p2, q2)), inv_zr);
+                    int rf = s_rflag[t2];
+                    if (s_tok[s_kids[t2]] == x) rf = 1;
+                    s_px[t2] = p2;
+                    s_qc[t2] = (rf || !ff_pos(sq)) ? ff_make(0.0f) : ff_mul_f(inv_sq, s_qx[t2]);
+                    s_rflag[t2] = rf;
+                }
             }
             __syncthreads();
             ++nrej;
@@ -637,8 +690,8 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
             } else {
                 // empty residual: p keeps its previous value, which the pass overwrote --
                 // rebuild it from the logits (unreachable in exact arithmetic)
-                rebuild_level<VEC, ALIGNED>(lv, lrow, qrow, v0, v1, nrej, M, T, invT, s_invz, s_xrej, s_inv_sq,
-                                            s_inv_zr, s_zr_ok);
+                rebuild_level<VEC, ALIGNED>(lv, lrow, qrow, v0, v1, nrej, c2, MC, invZf, s_xrej, s_inv_sq, s_inv_zr,
+                                            s_zr_ok);
                 lv_is_p = true;
                 pscale = 1.0f;
             }
@@ -649,6 +702,8 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
         node = next;
         __syncthreads();
     }
+
+    if (warp == nwarps - 1) asm volatile("cp.async.wait_all;" ::: "memory");  // no copies in flight at exit
 
     // ---- outputs
     const long long rowoff = (long long)b * N;
@@ -688,14 +743,13 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
 
     // ---- bonus: inverse CDF of the current p in token order.  Token order within a
     // CTA is (vector step k, warp, lane, element); prefix sums are float-float.
-    const float invZ = s_invz;
     float(&pk)[VEC][4] = lv;  // the slice is not needed after this pass
 #pragma unroll
     for (int k = 0; k < VEC; ++k)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
             const int v = v0 + (k * (int)blockDim.x + tid) * 4 + e;
-            const float p = lv_is_p ? lv[k][e] * pscale : expf(div_t(lv[k][e] - M, T, invT)) * invZ;
+            const float p = lv_is_p ? lv[k][e] * pscale : ex2(fmaf(lv[k][e], c2, -MC)) * invZf;
             pk[k][e] = (v < v1) ? p : 0.0f;
         }
 #pragma unroll
@@ -822,16 +876,27 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
 
 namespace tsv {
 
+// dynamic shared memory of the walk: aligned rows keep the node's draft row slice
+// (v_per_cta floats)
+template <bool ALIGNED>
+static size_t reject_smem(int vpc) {
+    return ALIGNED ? (size_t)vpc * sizeof(float) : 0;
+}
+
 template <int VEC, bool ALIGNED>
-static cudaError_t make_reject_config(int B, int cs, int threads, cudaStream_t stream, cudaLaunchConfig_t* cfg,
-                                      cudaLaunchAttribute* attr) {
+static cudaError_t make_reject_config(int B, int cs, int threads, int vpc, cudaStream_t stream,
+                                      cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr) {
     cudaError_t e = cudaFuncSetAttribute(tree_reject_kernel<VEC, ALIGNED>,
                                          cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+    const size_t smem = reject_smem<ALIGNED>(vpc);
+    e = cudaFuncSetAttribute(tree_reject_kernel<VEC, ALIGNED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     *cfg = cudaLaunchConfig_t{};
     cfg->gridDim = dim3((unsigned)(B * cs), 1, 1);
     cfg->blockDim = dim3((unsigned)threads, 1, 1);
-    cfg->dynamicSmemBytes = 0;
+    cfg->dynamicSmemBytes = smem;
     cfg->stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = (unsigned)cs;
@@ -846,26 +911,26 @@ template <int VEC, bool ALIGNED>
 static cudaError_t launch_reject_inst(const SampleArgs& a, int B, int cs, int threads, cudaStream_t stream) {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
-    cudaError_t e = make_reject_config<VEC, ALIGNED>(B, cs, threads, stream, &cfg, attr);
+    cudaError_t e = make_reject_config<VEC, ALIGNED>(B, cs, threads, a.v_per_cta, stream, &cfg, attr);
     if (e != cudaSuccess) return e;
     return cudaLaunchKernelEx(&cfg, tree_reject_kernel<VEC, ALIGNED>, a);
 }
 
 // How many clusters of this shape can be resident at once (cached per shape).
 template <int VEC, bool ALIGNED>
-static int resident_clusters(int cs, int threads) {
+static int resident_clusters(int cs, int threads, int vpc) {
     static std::mutex mu;
-    static std::map<std::pair<int, int>, int> cache;
+    static std::map<std::pair<long long, int>, int> cache;
     std::lock_guard<std::mutex> lock(mu);
     int dev = 0;
     cudaGetDevice(&dev);
-    const auto key = std::make_pair(dev * 64 + cs, threads);
+    const auto key = std::make_pair(((long long)dev * 64 + cs) * (1LL << 32) + vpc, threads);
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     int n = 0;
-    if (make_reject_config<VEC, ALIGNED>(1, cs, threads, nullptr, &cfg, attr) != cudaSuccess ||
+    if (make_reject_config<VEC, ALIGNED>(1, cs, threads, vpc, nullptr, &cfg, attr) != cudaSuccess ||
         cudaOccupancyMaxActiveClusters(&n, tree_reject_kernel<VEC, ALIGNED>, &cfg) != cudaSuccess)
         n = 0;
     cache[key] = n;
@@ -881,12 +946,12 @@ static int vec_for(int V, int cs, int threads, int* vpc_out) {
 }
 
 template <bool ALIGNED>
-static int resident_for(int vec, int cs, int threads) {
+static int resident_for(int vec, int cs, int threads, int vpc) {
     switch (vec) {
-        case 1: return resident_clusters<1, ALIGNED>(cs, threads);
-        case 2: return resident_clusters<2, ALIGNED>(cs, threads);
-        case 4: return resident_clusters<4, ALIGNED>(cs, threads);
-        default: return resident_clusters<8, ALIGNED>(cs, threads);
+        case 1: return resident_clusters<1, ALIGNED>(cs, threads, vpc);
+        case 2: return resident_clusters<2, ALIGNED>(cs, threads, vpc);
+        case 4: return resident_clusters<4, ALIGNED>(cs, threads, vpc);
+        default: return resident_clusters<8, ALIGNED>(cs, threads, vpc);
     }
 }
 
@@ -911,7 +976,7 @@ cudaError_t launch_tree_reject(SampleArgs a, int B, int num_sms, cudaStream_t st
     while (cs > cs_min) {
         int vpc;
         const int vec = vec_for(V, cs, threads, &vpc);
-        const int res = aligned ? resident_for<true>(vec, cs, threads) : resident_for<false>(vec, cs, threads);
+        const int res = aligned ? resident_for<true>(vec, cs, threads, vpc) : resident_for<false>(vec, cs, threads, vpc);
         if (res >= B && B * cs <= 2 * num_sms) break;
         cs >>= 1;
     }
