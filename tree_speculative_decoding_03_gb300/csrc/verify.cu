@@ -83,6 +83,12 @@ __device__ __forceinline__ ff ff_mul(ff a, ff b) {
     e = fmaf(a.hi, b.lo, fmaf(a.lo, b.hi, e));
     return quick_two_sum(p, e);
 }
+// 1 / b: a correctly rounded reciprocal of b.hi refined by one float-float step
+__device__ __forceinline__ ff ff_recip(ff b) {
+    const float q1 = __frcp_rn(b.hi);
+    const ff r = ff_sub(ff_make(1.0f), ff_mul_f(b, q1));
+    return quick_two_sum(q1, r.hi * q1);
+}
 __device__ __forceinline__ ff ff_div(ff a, ff b) {
     const float q1 = a.hi / b.hi;
     const ff r = ff_sub(a, ff_mul_f(b, q1));
@@ -243,16 +249,20 @@ enum { kRedStats = 0, kRedSums = 1, kRedArgmax = 2 };
 // (a, i).  Must be called by every thread of every CTA; the result is in *res
 // after the closing __syncthreads.  Slots alternate by parity, so the write of the
 // next reduction cannot overtake a slow CTA still reading this one.
+struct NoPost {
+    __device__ void operator()(const RedSlot&) const {}
+};
+template <typename Post = NoPost>
 __device__ __forceinline__ void cluster_allreduce(cg::cluster_group& cluster, RedSlot* slots, int parity,
                                                   const RedSlot& mine, int kind, float c2, RedSlot* res,
-                                                  bool wait_async = false) {
+                                                  bool wait_async = false, const Post& post = Post()) {
     const int tid = threadIdx.x, lane = tid & 31;
     const int cs = (int)cluster.num_blocks();
     if (tid == 0) slots[parity] = mine;
-    cluster.sync();
-    // the last warp's asynchronous copies land while the cluster combines; the closing
-    // barrier makes them visible to the whole CTA
+    // the last warp's asynchronous copies (issued before the row pass) have landed by the
+    // cluster barrier, which makes them visible to warp 0's post-step
     if (wait_async && (tid >> 5) == (int)(blockDim.x >> 5) - 1) asm volatile("cp.async.wait_all;" ::: "memory");
+    cluster.sync();
     if (tid < 32) {
         RedSlot r{};
         r.a = -INFINITY;
@@ -286,6 +296,7 @@ __device__ __forceinline__ void cluster_allreduce(cg::cluster_group& cluster, Re
             o.i = i;
         }
         if (lane == 0) *res = o;
+        post(o);  // warp 0, every lane holds the combined result
     }
     __syncthreads();
 }
@@ -512,23 +523,19 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                 }
             }
             __syncthreads();
-            cluster_allreduce(cluster, s_red, parity, s_cta, kRedStats, c2, &s_all, true);
-            parity ^= 1;
-            M = s_all.a;
-            MC = M * c2;
-            const ff Zf{s_all.hi, s_all.lo};
-            invZf = 1.0f / ff_float(Zf);
-            // the ratio's normaliser: sum of exp((l - M) / T), i.e. Zf without the rounding of M c2
-            const ff Z = ff_mul_f(Zf, exp2f(-fmaf(M, c2, -MC)));
-            const ff invZ = ff_div(ff_make(1.0f), Z);
-            // children's p(x), q(x) at level 0, one lane per child (p(x) in float-float from
-            // a compensated exponent argument)
-            if (warp == 0) {
+            // warp 0, before the reduction's closing barrier: the children's p(x), q(x) at
+            // level 0, one lane per child (p(x) in float-float from a compensated exponent
+            // argument; the normaliser is Zf without the rounding of M c2).  The last warp's
+            // copies of the children's scalars have landed by the cluster barrier.
+            auto children_p = [&](const RedSlot& o) {
+                const float Mo = o.a, MCo = Mo * c2;
+                const ff Z = ff_mul_f(ff{o.hi, o.lo}, exp2f(-fmaf(Mo, c2, -MCo)));
+                const ff invZ = ff_recip(Z);
                 for (int t = lane; t < nk; t += 32) {
                     const float qraw = s_qx[t];
                     ff px = ff_make(0.0f);
                     if (isfinite(qraw)) {
-                        const ff arg = ff_mul(two_sum(s_lx[t], -M), invT_ff);
+                        const ff arg = ff_mul(two_sum(s_lx[t], -Mo), invT_ff);
                         const float ex = expf(arg.hi);
                         px = ff_mul(quick_two_sum(ex, ex * arg.lo), invZ);
                     }
@@ -536,13 +543,17 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                     s_qc[t] = ff_make(qraw);
                     s_rflag[t] = 0;
                 }
-            }
+            };
+            cluster_allreduce(cluster, s_red, parity, s_cta, kRedStats, c2, &s_all, true, children_p);
+            parity ^= 1;
+            M = s_all.a;
+            MC = M * c2;
+            invZf = 1.0f / ff_float(ff{s_all.hi, s_all.lo});
         }
         if (s_all.flag) {
             err = TSV_DERR_NONFINITE;
             break;
         }
-        __syncthreads();
 
         // ---- children, in index order
         nrej = 0;
@@ -669,8 +680,8 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                     s_sq[j] = sq;
                     s_inv_sq[j] = ff_pos(sq) ? ff_float(ff_div(ff_make(1.0f), sq)) : 0.0f;
                 }
-                const ff inv_zr = zr_ok ? ff_div(ff_make(1.0f), zr_new) : ff_make(1.0f);
-                const ff inv_sq = ff_pos(sq) ? ff_div(ff_make(1.0f), sq) : ff_make(0.0f);
+                const ff inv_zr = zr_ok ? ff_recip(zr_new) : ff_make(1.0f);
+                const ff inv_sq = ff_pos(sq) ? ff_recip(sq) : ff_make(0.0f);
                 for (int t2 = t + 1 + lane; t2 < nk; t2 += 32) {
                     ff p2 = s_px[t2];
                     const ff q2 = s_qc[t2];
