@@ -2,7 +2,8 @@
 """Benchmark of one tree-verification step on GB300.
 
 A step is one pass of the whole hot path over one synthetic batch, on one CUDA
-stream: tsv_tree_verify_attn (tree-masked attention + split-K merge),
+stream: tsv_tree_verify_attn (sequence checks, tree-masked attention over a
+persistent even split of all K/V tiles, merge of split units),
 tsv_tree_reject_sample (rejection-sampling walk + bonus token) and
 tsv_kv_compact_accepted (KV rewrite of the accepted path).
 
@@ -359,7 +360,9 @@ def run_ours(args, rank, world, local_rank):
     e2e = {"value": whole_job_rate(tokens_per_step * K, e2e_s, world), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
            "d2h_bytes_per_step": int(d2h)}
 
-    launches_per_step = 3 + (1 if ws_bytes else 0)
+    # bf16: check, persistent attention and merge kernels; fp32: attention (+ merge when split)
+    attn_launches = 3 if inp["dtype"] == "bf16" else 1 + (1 if ws_bytes else 0)
+    launches_per_step = attn_launches + 2
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": float(step_ms.mean()), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
