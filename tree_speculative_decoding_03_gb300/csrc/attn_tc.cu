@@ -15,10 +15,11 @@
 // loaded from HBM feeds Gq * N rows.  A CTA walks its tiles as segments, one per unit
 // it touches; a segment that covers its whole unit writes the output directly, the
 // others write (m, l, O / l) partials to a per-CTA slot, which a merge kernel over all
-// SMs combines (log-sum-exp).  A small kernel run first checks every sequence (flags,
-// NaN rows); flagged sequences get no tiles.  The three kernels are chained with
-// programmatic dependent launch, so each one's launch and set-up overlap the tail of
-// the one before.
+// SMs combines (log-sum-exp).  A small kernel checks every sequence (seq_err) while the
+// attention runs: the schedule depends only on the lengths, a flagged sequence's tiles
+// are computed anyway (reads stay inside the cache: out-of-range tensor-map boxes read
+// zeros) and the merge kernel, which runs after both, writes its rows as NaN.  The
+// kernels are chained with programmatic dependent launch.
 //
 // Warp roles (384 threads):
 //   warp 0      TMA producer: 128-key K and V tiles of the paged cache, one box per
@@ -40,8 +41,6 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
-
-#include <utility>
 
 #include "attn_common.cuh"
 #include "common.cuh"
@@ -214,11 +213,6 @@ __device__ __forceinline__ uint32_t sw128_offset(int row, int q) {
     return static_cast<uint32_t>(half * kHalfBytes + (row >> 3) * 1024 + (row & 7) * 128 + ((cc ^ (row & 7)) << 4));
 }
 
-// programmatic dependent launch: let the next kernel in the stream start launching /
-// wait until the previous kernel has completed and its writes are visible
-__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
@@ -261,15 +255,13 @@ struct Bars {
 // segment parity), per-slot fill metadata, the CTA's schedule
 constexpr uint32_t kMiscPar = 0, kMiscMeta = 256, kMiscSched = 320;
 
-// Tiles of each unit of sequence b: 0 for a sequence the check kernel flagged (or
-// whose length does not fit the block table), else ceil((L_b + N) / 128).  The
-// timeout bit, which a CTA of this kernel may set while others read, is ignored, so
-// every thread sees the same schedule.
+// Tiles of each unit of sequence b: 0 when its length does not fit the block table
+// (so no block-table entry past the row is read), else ceil((L_b + N) / 128).  It depends
+// on the lengths only, so it needs nothing from the check kernel running alongside.
 __device__ __forceinline__ int seq_tiles(const AttnArgs& a, int b, int* L_out) {
     const int L = __ldg(a.seq_lens + b);
-    const int e = a.seq_err[b] & ~TSV_DERR_TIMEOUT;
     *L_out = L;
-    if (e != 0 || L < 0 || (long long)L + a.N > ((long long)a.max_blocks << a.bs_log2)) return 0;
+    if (L < 0 || (long long)L + a.N > ((long long)a.max_blocks << a.bs_log2)) return 0;
     return (L + a.N + kTileKeys - 1) / kTileKeys;
 }
 
@@ -356,11 +348,13 @@ __device__ __forceinline__ void find_start(const AttnArgs& a, int lane_c, int* s
     }
 }
 
-// One CTA per sequence, run before the attention kernel: the checks behind seq_err[b]
-// (capacity first; a parent array that is not a tree; a block id outside the cache)
-// and NaN rows for a flagged sequence.
+// One CTA per sequence, alongside the attention kernel: the checks behind seq_err[b]
+// (capacity first; a parent array that is not a tree; a block id outside the cache).
 __global__ void __launch_bounds__(128) attn_tc_check_kernel(const AttnArgs a) {
     __shared__ int s_flag;
+    // the inputs may come from the previous kernel in the stream: wait for it before the
+    // attention kernel (which reads them too) is allowed to start
+    pdl_wait();
     pdl_launch_dependents();
     const int b = blockIdx.x, N = a.N;
     const int L = a.seq_lens[b];
@@ -371,11 +365,6 @@ __global__ void __launch_bounds__(128) attn_tc_check_kernel(const AttnArgs a) {
         e |= block_cache_errors(a.block_table + (long long)b * a.max_blocks, L, N, 1 << a.bs_log2, a.max_blocks,
                                 a.num_blocks, &s_flag);
     if (threadIdx.x == 0) a.seq_err[b] = e;
-    if (e) {
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(a.out) + (long long)b * N * a.Hq * a.D;
-        const __nv_bfloat16 nan = __float2bfloat16_rn(__int_as_float(0x7fc00000));
-        for (long long i = threadIdx.x; i < (long long)N * a.Hq * a.D; i += blockDim.x) out[i] = nan;
-    }
 }
 
 template <int D>
@@ -425,8 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(smem_u32(s_tmem), 512);
         tmem_relinquish();
     }
-    pdl_launch_dependents();
-    pdl_wait();  // seq_err comes from the check kernel
+    pdl_launch_dependents();  // the check kernel before it has started: the schedule needs nothing from it
     if (warp == 2) find_start(a, lane_c, s_sched);
     tc_fence_before();
     __syncthreads();
@@ -898,6 +886,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) my_err = 1;
     }
+    // the check kernel has written seq_err before this CTA completes (and so before the
+    // merge kernel runs, or a timeout flag is added to it)
+    pdl_wait();
     if (my_err) {
         *s_abort = 1;
         atomicOr(&a.seq_err[err_b], TSV_DERR_TIMEOUT);
@@ -916,6 +907,7 @@ template <int D>
 __global__ void __launch_bounds__(256) attn_tc_merge_kernel(const AttnArgs a) {
     constexpr int C = D / 8;  // columns per thread
     pdl_wait();
+    pdl_launch_dependents();
     const int nrg = a.n_rgroups;
     const int u = blockIdx.x;
     const int rg = u % nrg, g = (u / nrg) % a.Hkv, b = u / (nrg * a.Hkv);
@@ -923,7 +915,20 @@ __global__ void __launch_bounds__(256) attn_tc_merge_kernel(const AttnArgs a) {
     const int e = a.seq_err[b];
     const int c_first = ui[0], c_last = ui[1], sd0 = ui[2];
     const long long T_all = reinterpret_cast<const long long*>(ui)[2];
-    if (e != 0) return;  // flagged (NaN rows) or timed out
+    if (e & ~TSV_DERR_TIMEOUT) {  // flagged by the check kernel: this block's rows become NaN
+        const int r_base = rg * 256, rows_rg = min(256, a.R - r_base);
+        const int rr = blockIdx.y * 32 + (threadIdx.x >> 3), c0 = (threadIdx.x & 7) * C;
+        if (rr < rows_rg) {
+            const int r = r_base + rr;
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out) +
+                                 (((long long)b * a.N + r / a.G) * a.Hq + g * a.G + r % a.G) * D + c0;
+            const __nv_bfloat16 nan = __float2bfloat16_rn(__int_as_float(0x7fc00000));
+#pragma unroll
+            for (int q = 0; q < C; ++q) dst[q] = nan;
+        }
+        return;
+    }
+    if (e != 0) return;  // timed out: outputs are not valid
     if (c_last <= c_first || c_first < 0 || c_last >= a.lanes || T_all < 1) return;  // one piece: written directly
     const int r_base = rg * 256;
     const int rows_rg = min(256, a.R - r_base);
@@ -1015,24 +1020,6 @@ __global__ void __launch_bounds__(256) attn_tc_merge_kernel(const AttnArgs a) {
     }
 }
 
-// launches `kernel` with programmatic stream serialisation: it may start while the
-// previous kernel in the stream finishes, and waits for it with griddepcontrol.wait
-template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                       Args&&... args) {
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
-}
-
 PFN_cuTensorMapEncodeTiled_v12000 get_encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
@@ -1088,8 +1075,7 @@ cudaError_t launch_tc_inst(const AttnArgs& a, cudaStream_t stream) {
     }
     const CUtensorMap& mk = mc.mk;
     const CUtensorMap& mv = mc.mv;
-    attn_tc_check_kernel<<<static_cast<unsigned>(a.B), 128, 0, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(attn_tc_check_kernel, dim3(static_cast<unsigned>(a.B)), dim3(128), 0, stream, 1u, a);
     if (e != cudaSuccess) return e;
     const int nm_max = a.R > 128 ? 2 : 1;
     const TcLayout lay = tc_layout<D>(nm_max);
@@ -1106,11 +1092,11 @@ cudaError_t launch_tc_inst(const AttnArgs& a, cudaStream_t stream) {
         smem_set = static_cast<int>(lay.total);
     }
     e = launch_pdl(attn_tc_kernel<D>, dim3(static_cast<unsigned>(a.lanes * a.n_rgroups)), dim3(kThreads), lay.total,
-                   stream, a, mk, mv, nm_max);
+                   stream, 1u, a, mk, mv, nm_max);
     if (e != cudaSuccess) return e;
     return launch_pdl(attn_tc_merge_kernel<D>,
                       dim3(static_cast<unsigned>(a.B * a.Hkv * a.n_rgroups), static_cast<unsigned>((a.rows_item + 31) / 32)),
-                      dim3(256), 0, stream, a);
+                      dim3(256), 0, stream, 1u, a);
 }
 
 }  // namespace

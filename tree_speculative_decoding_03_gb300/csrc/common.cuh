@@ -2,6 +2,8 @@
 #pragma once
 
 #include <cstdint>
+#include <utility>
+
 #include <cuda_runtime.h>
 
 #include "../../include/tsv.h"
@@ -9,6 +11,40 @@
 namespace tsv {
 
 constexpr int kMaxNodes = 128;  // tree nodes per sequence, root included
+
+// Programmatic dependent launch: every kernel of the library lets the next kernel in the
+// stream start launching early (pdl_launch_dependents) and waits for the previous one to
+// complete, with its writes visible, before reading anything (pdl_wait).  Without the
+// launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Launches `kernel` with programmatic stream serialisation (it may start while the
+// previous kernel in the stream finishes; it waits for it with pdl_wait), plus an
+// optional cluster shape.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              unsigned cluster_x, Args&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    int n = 1;
+    if (cluster_x > 1) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = cluster_x;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        n = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Validates one sequence's tree: parent[0] == -1 and 0 <= parent[i] < i.
 // Cooperative over the calling block; every thread gets the same answer.

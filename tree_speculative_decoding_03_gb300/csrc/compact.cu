@@ -23,6 +23,8 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(
     int bs_log2, int max_blocks, int num_blocks, int32_t* __restrict__ seq_err) {
     __shared__ int s_flag;
     __shared__ int s_path[kMaxNodes];
+    pdl_wait();  // accepted paths come from the previous kernel
+    pdl_launch_dependents();
     const int b = blockIdx.x;
     const int L = seq_lens[b];
     const int A = accept_len[b];
@@ -92,10 +94,10 @@ cudaError_t launch_kv_compact(void* k_cache, void* v_cache, const int32_t* block
     if (B == 0) return cudaSuccess;
     int bs_log2 = 0;
     while ((1 << bs_log2) < block_size) ++bs_log2;
-    kv_compact_kernel<<<B, 256, 0, stream>>>(static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache),
-                                             block_table, seq_lens, accepted_nodes, accept_len, new_seq_lens, N,
-                                             Hkv * D * elem_bytes, bs_log2, max_blocks, num_blocks, seq_err);
-    return cudaGetLastError();
+    return launch_pdl(kv_compact_kernel, dim3(static_cast<unsigned>(B)), dim3(256), 0, stream, 1u,
+                      static_cast<uint8_t*>(k_cache), static_cast<uint8_t*>(v_cache), block_table, seq_lens,
+                      accepted_nodes, accept_len, new_seq_lens, N, Hkv * D * elem_bytes, bs_log2, max_blocks,
+                      num_blocks, seq_err);
 }
 
 }  // namespace tsv

@@ -329,6 +329,8 @@ __device__ __forceinline__ void rebuild_level(float (&lv)[VEC][4], const float* 
 
 template <int VEC, bool ALIGNED>
 __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a) {
+    pdl_wait();  // the inputs may come from the previous kernel in the stream
+    pdl_launch_dependents();
     cg::cluster_group cluster = cg::this_cluster();
     const int cs = (int)cluster.num_blocks();
     const int rank = (int)cluster.block_rank();
@@ -924,7 +926,8 @@ static cudaError_t launch_reject_inst(const SampleArgs& a, int B, int cs, int th
     cudaLaunchAttribute attr[1];
     cudaError_t e = make_reject_config<VEC, ALIGNED>(B, cs, threads, a.v_per_cta, stream, &cfg, attr);
     if (e != cudaSuccess) return e;
-    return cudaLaunchKernelEx(&cfg, tree_reject_kernel<VEC, ALIGNED>, a);
+    return launch_pdl(tree_reject_kernel<VEC, ALIGNED>, cfg.gridDim, cfg.blockDim, cfg.dynamicSmemBytes, stream,
+                      static_cast<unsigned>(cs), a);
 }
 
 // How many clusters of this shape can be resident at once (cached per shape).
