@@ -982,17 +982,19 @@ cudaError_t launch_tree_reject(SampleArgs a, int B, int num_sms, cudaStream_t st
     while (cs_min * cap1 < V) cs_min *= 2;  // smallest cluster that fits the row
     const bool aligned = (V % 4) == 0 && (reinterpret_cast<uintptr_t>(a.logits) & 15) == 0 &&
                          (a.probs == nullptr || (reinterpret_cast<uintptr_t>(a.probs) & 15) == 0);
-    // Enough CTAs that a thread holds at most 16 entries (VEC <= 4): longer rows per
-    // thread make every pass slower, more CTAs make every cluster barrier slower.  A
-    // larger cluster is kept only if all B clusters can be resident at once.
+    // Enough CTAs that a thread holds at most 8 entries: every visited node costs a
+    // pass over the slice, and the slice load dominates it.  A cluster larger than the
+    // smallest that fits the row is kept only if all B clusters can be resident at once
+    // (sizes between powers of two are tried too: 16-CTA clusters need 16 free SMs in
+    // one GPC, which not every GPC has).
     int cs = cs_min;
-    while (cs < 16 && cs * threads * 16 < V) cs *= 2;
-    while (cs > cs_min) {
+    while (cs < 16 && cs * threads * 8 < V) cs *= 2;
+    for (; cs > cs_min; --cs) {
         int vpc;
         const int vec = vec_for(V, cs, threads, &vpc);
+        if (vec == 0) continue;
         const int res = aligned ? resident_for<true>(vec, cs, threads, vpc) : resident_for<false>(vec, cs, threads, vpc);
-        if (res >= B && B * cs <= 2 * num_sms) break;
-        cs >>= 1;
+        if (res >= B && B * cs <= num_sms) break;
     }
     int vpc;
     const int vec = vec_for(V, cs, threads, &vpc);
