@@ -252,8 +252,8 @@ struct Bars {
 };
 
 // misc region (512 bytes): parents of the segment's sequence (int8, two buffers by
-// segment parity), per-slot fill metadata, the CTA's schedule
-constexpr uint32_t kMiscPar = 0, kMiscMeta = 256, kMiscSched = 320;
+// segment parity), per-slot fill metadata, the CTA's schedule, the first tile's block ids
+constexpr uint32_t kMiscPar = 0, kMiscMeta = 256, kMiscSched = 320, kMiscBlk0 = 384;
 
 // Tiles of each unit of sequence b: 0 when its length does not fit the block table
 // (so no block-table entry past the row is read), else ceil((L_b + N) / 128).  It depends
@@ -292,15 +292,23 @@ __device__ __forceinline__ int lane_of_tile(long long x, long long T, int lanes)
 }
 __device__ __forceinline__ long long lane_start(int k, long long T, int lanes) { return (long long)k * T / lanes; }
 
-// One warp: total tiles, this lane's run [s, e) and the unit/tile where it starts.
-// sched: b, g, t, Tb, L, count, s (2 words), T (2 words).
-__device__ __forceinline__ void find_start(const AttnArgs& a, int lane_c, int* sched) {
+// One warp: total tiles, this lane's run [s, e), the unit/tile where it starts and
+// the block ids of that first tile (so the first copies need no global read after the
+// set-up barrier).  sched: b, g, t, Tb, L, count, s (2 words), T (2 words);
+// blk0[j] = id of the first tile's j-th cache block (j < 16).
+__device__ __forceinline__ void find_start(const AttnArgs& a, int lane_c, int* sched, int* blk0) {
     const int lane = threadIdx.x & 31;
     long long T = 0;
+    int tb_first = 0, L_first = 0;  // the first 32 sequences, kept for the second pass
     for (int b0 = 0; b0 < a.B; b0 += 32) {
-        int L;
+        int L = 0;
         const int b = b0 + lane;
-        T += b < a.B ? seq_tiles(a, b, &L) : 0;
+        const int tb = b < a.B ? seq_tiles(a, b, &L) : 0;
+        if (b0 == 0) {
+            tb_first = tb;
+            L_first = L;
+        }
+        T += tb;
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) T += __shfl_xor_sync(0xffffffffu, T, o);
@@ -310,9 +318,9 @@ __device__ __forceinline__ void find_start(const AttnArgs& a, int lane_c, int* s
     if (e > s) {
         long long base = 0;
         for (int b0 = 0; b0 < a.B; b0 += 32) {
-            int L = 0;
+            int L = L_first;
             const int b = b0 + lane;
-            const int tb = b < a.B ? seq_tiles(a, b, &L) : 0;
+            const int tb = b0 == 0 ? tb_first : (b < a.B ? seq_tiles(a, b, &L) : 0);
             const long long w = (long long)tb * a.Hkv;
             long long incl = w;
 #pragma unroll
@@ -345,6 +353,11 @@ __device__ __forceinline__ void find_start(const AttnArgs& a, int lane_c, int* s
         sched[5] = static_cast<int>(e - s);
         reinterpret_cast<long long*>(sched)[3] = s;  // words 6-7
         reinterpret_cast<long long*>(sched)[4] = T;  // words 8-9
+    }
+    if (e > s && lane < 16) {
+        const int u0 = ft * kTileKeys;
+        const int nb = (min(u0 + kTileKeys, fL + a.N) - u0 + (1 << a.bs_log2) - 1) >> a.bs_log2;
+        blk0[lane] = lane < nb ? __ldg(a.block_table + (long long)fb * a.max_blocks + (u0 >> a.bs_log2) + lane) : 0;
     }
 }
 
@@ -381,6 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int8_t* s_par = reinterpret_cast<int8_t*>(smem + lay.misc + kMiscPar);  // [2][128]
     volatile int* s_meta = reinterpret_cast<volatile int*>(smem + lay.misc + kMiscMeta);  // [kMaxSlots]
     int* s_sched = reinterpret_cast<int*>(smem + lay.misc + kMiscSched);
+    int* s_blk0 = reinterpret_cast<int*>(smem + lay.misc + kMiscBlk0);  // [16]
     volatile int* s_abort = reinterpret_cast<volatile int*>(smem + lay.bars + 8 * Bars::kCount);
     uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + lay.bars + 8 * Bars::kCount + 4);
     const uint32_t bar0 = smem_u32(bars);
@@ -415,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     pdl_launch_dependents();  // the check kernel before it has started: the schedule needs nothing from it
-    if (warp == 2) find_start(a, lane_c, s_sched);
+    if (warp == 2) find_start(a, lane_c, s_sched, s_blk0);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -430,12 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the tile's j-th cache block and issues that block's boxes).  The next tile's
         // block ids are loaded while the current tile's fills wait for their slots.
         TileIt it = it0;
-        int blk = 0;
-        if (count > 0) {
-            const int u0 = it.t * kTileKeys;
-            const int nb = (min(u0 + kTileKeys, it.L + N) - u0 + bs - 1) >> a.bs_log2;
-            blk = lane < nb ? __ldg(a.block_table + (long long)it.b * a.max_blocks + (u0 >> a.bs_log2) + lane) : 0;
-        }
+        int blk = (count > 0 && lane < 16) ? s_blk0[lane] : 0;  // looked up during set-up
         int seg = 0;
         for (int jt = 0; jt < count && !my_err; ++jt) {
             if (jt > 0 && it.t == 0) ++seg;
