@@ -86,8 +86,10 @@ const char *tsv_last_error(void);
  * block_size a power of two in [8, 128].
  * bf16: persistent CTAs split the 128-key tiles of all (sequence, kv head) pairs
  * evenly; a pair that straddles CTAs leaves partial (max, sum, output) in
- * `workspace`, merged by the CTA that finishes its last piece.  fp32: long prefixes
- * are split into key chunks whose partials are merged by a second kernel.
+ * `workspace`, combined by a merge kernel.  fp32: long prefixes are split into key
+ * chunks whose partials are merged by a second kernel.  The call's kernels are
+ * chained with programmatic dependent launch; each waits for the kernel before it
+ * in the stream to complete before reading its inputs.
  * `workspace` must hold tsv_attn_workspace_size(...) bytes (may be NULL when that
  * is 0); it is scratch owned by the caller, and every byte the call reads there is
  * written earlier in the same call (no clearing needed between calls).

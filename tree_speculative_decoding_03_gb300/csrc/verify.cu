@@ -17,8 +17,8 @@
 // (fp32) -> one warp per CTA -> DSMEM across the cluster; every CTA combines the
 // cluster partials in the same order, so all CTAs hold bit-identical scalars and
 // take identical decisions without a second exchange.  The first child's logits
-// row and the node's draft row are prefetched into L2 while the current row is
-// reduced.
+// row is prefetched into L2 while the current row is reduced, and the children's
+// scalars are copied asynchronously (cp.async) while it is reduced.
 //
 // Precision without fp64: GB300's fp64 rate is a small fraction of fp32, so sums
 // across threads, warps and CTAs are carried as float-float pairs (error-free
