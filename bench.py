@@ -3,9 +3,9 @@
 
 A step is one pass of the whole hot path over one synthetic batch, on one CUDA
 stream: tsv_tree_verify_attn (sequence checks, tree-masked attention over a
-persistent even split of all K/V tiles, merge of split units),
-tsv_tree_reject_sample (rejection-sampling walk + bonus token) and
-tsv_kv_compact_accepted (KV rewrite of the accepted path).
+persistent even split of all K/V tiles, merge of split units) and
+tsv_tree_reject_sample_compact (rejection-sampling walk + bonus token, with the KV
+rewrite of the accepted path in the same launch).
 
 Metric: verified draft-tree tokens per second = B * N tree tokens (root included)
 per step / device time per step.  The workload defaults to the chain
@@ -282,14 +282,13 @@ def run_ours(args, rank, world, local_rank):
                              Dv["parent"], out, inp["scale"], workspace=ws if ws_bytes else None, seq_err=attn_err)
         if ev is not None:
             ev[1].record(stream)
-        tsv.tree_reject_sample(Dv["target_logits"], Dv["draft_probs"], Dv["draft_tokens"], Dv["parent"],
-                               Dv["u_accept"], Dv["u_bonus"], T, acc_nodes, acc_len, bonus, out_tokens, samp_err)
+        # the walk with the KV-cache rewrite of its accepted path in its tail
+        tsv.tree_reject_sample_compact(Dv["target_logits"], Dv["draft_probs"], Dv["draft_tokens"], Dv["parent"],
+                                       Dv["u_accept"], Dv["u_bonus"], T, acc_nodes, acc_len, bonus, out_tokens,
+                                       samp_err, Dv["k_cache"], Dv["v_cache"], Dv["block_table"], Dv["seq_lens"],
+                                       new_lens, comp_err)
         if ev is not None:
             ev[2].record(stream)
-        tsv.kv_compact_accepted(Dv["k_cache"], Dv["v_cache"], Dv["block_table"], Dv["seq_lens"], acc_nodes,
-                                acc_len, new_lens, comp_err)
-        if ev is not None:
-            ev[3].record(stream)
 
     flush = torch.empty(64 * 1024 * 1024, dtype=torch.float32, device="cuda")  # 256 MB > 129 MB L2
     for i in range(args.warmup):
@@ -304,7 +303,7 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize()
 
     K = args.steps
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
     with ClockSampler(local_rank) as clk:
         barrier()
         t_wall = time.perf_counter()
@@ -314,7 +313,7 @@ def run_ours(args, rank, world, local_rank):
         barrier()
         t_wall = time.perf_counter() - t_wall
     clocks = clk.summary(0, 0)
-    per = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in evs])  # ms
+    per = np.array([[e[i].elapsed_time(e[i + 1]) for i in range(2)] for e in evs])  # ms
     step_ms = per.sum(axis=1)
     dev_s = float(step_ms.sum()) / 1e3
     tokens_per_step = B * N
@@ -325,8 +324,7 @@ def run_ours(args, rank, world, local_rank):
     mean_ms = per.mean(axis=0)
     kernels = {
         "tree_verify_attn": (attn_bytes(inp), mean_ms[0]),
-        "tree_reject_sample": (verify_bytes(inp, an, al), mean_ms[1]),
-        "kv_compact_accepted": (compact_bytes(inp, al), mean_ms[2]),
+        "tree_reject_sample_compact": (verify_bytes(inp, an, al) + compact_bytes(inp, al), mean_ms[1]),
     }
     dom = max(kernels, key=lambda k: kernels[k][1])
     peak, peak_kind = _peaks()
@@ -362,7 +360,7 @@ def run_ours(args, rank, world, local_rank):
 
     # bf16: check, persistent attention and merge kernels; fp32: attention (+ merge when split)
     attn_launches = 3 if inp["dtype"] == "bf16" else 1 + (1 if ws_bytes else 0)
-    launches_per_step = attn_launches + 2
+    launches_per_step = attn_launches + 1  # + the walk with its fused rewrite
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": float(step_ms.mean()), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,

@@ -8,7 +8,8 @@
  *                                 paged KV cache under the ancestor-only tree mask;
  *   2. tsv_tree_reject_sample  -- rejection-sampling walk of the tree (Sequoia-style
  *                                 sampling without replacement) plus a bonus token;
- *   3. tsv_kv_compact_accepted -- KV-cache rewrite of the accepted path.
+ *   3. tsv_kv_compact_accepted -- KV-cache rewrite of the accepted path
+ *      (tsv_tree_reject_sample_compact runs 2 and 3 in one launch).
  * (Step 2 consumes target logits, which in a full model are produced from step
  * 1's output by the layers above attention; the library takes them as input.)
  *
@@ -187,6 +188,25 @@ tsv_status tsv_kv_compact_accepted(void *k_cache, void *v_cache, const int32_t *
                                    const int32_t *accept_len, int32_t *new_seq_lens, int B, int N,
                                    int Hkv, int D, int block_size, int max_blocks, int num_blocks,
                                    tsv_dtype dtype, int32_t *seq_err, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * The walk and the KV-cache rewrite in one launch: the same arguments and results as
+ * tsv_tree_reject_sample(...) followed by tsv_kv_compact_accepted(k_cache, v_cache,
+ * block_table, seq_lens, accepted_nodes, accept_len, new_seq_lens, ..., compact_err)
+ * on the same stream (the rewrite runs in the walk kernel's tail, one CTA per
+ * sequence, so it costs no launch of its own).  Walk errors go to seq_err, rewrite
+ * errors to compact_err, with the same codes as the two calls.
+ * ------------------------------------------------------------------------- */
+tsv_status tsv_tree_reject_sample_compact(const float *target_logits, const float *draft_probs,
+                                          const int32_t *draft_tokens, const int32_t *parent,
+                                          const float *u_accept, const float *u_bonus,
+                                          float temperature, int B, int N, int V,
+                                          int32_t *accepted_nodes, int32_t *accept_len,
+                                          int32_t *bonus_token, int32_t *out_tokens, int32_t *seq_err,
+                                          void *k_cache, void *v_cache, const int32_t *block_table,
+                                          const int32_t *seq_lens, int32_t *new_seq_lens, int Hkv,
+                                          int D, int block_size, int max_blocks, int num_blocks,
+                                          tsv_dtype dtype, int32_t *compact_err, void *stream);
 
 #ifdef __cplusplus
 }

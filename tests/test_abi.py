@@ -40,7 +40,26 @@ def test_host_argument_checks_need_no_gpu(lib):
     assert st == tsv.TSV_ERR_UNSUPPORTED  # block size 12
     # empty batch is a no-op
     assert lib.tsv_kv_compact_accepted(P, P, P, P, P, P, P, 0, 8, 2, 64, 16, 4, 8, 0, P, P) == tsv.TSV_OK
+    # the fused walk + rewrite checks both calls' arguments
+    fused = lib.tsv_tree_reject_sample_compact
+    walk = [P] * 6
+    assert fused(*walk, 1.0, 4, 200, 100, *[P] * 5, *[P] * 5, 2, 64, 16, 4, 8, 0, P, P) == tsv.TSV_ERR_UNSUPPORTED
+    assert fused(*walk, 1e-8, 4, 8, 100, *[P] * 5, *[P] * 5, 2, 64, 16, 4, 8, 0, P, P) == tsv.TSV_ERR_UNSUPPORTED
+    fake = [16] * 5  # non-null, never dereferenced: the call is refused before any launch
+    assert fused(*[16] * 6, 0.0, 4, 8, 100, *fake, *fake, 2, 64, 12, 4, 8, 0, 16, P) == tsv.TSV_ERR_UNSUPPORTED
+    assert fused(*[16] * 6, 0.0, 4, 8, 100, *fake, *[P] * 5, 2, 64, 16, 4, 8, 0, P, P) == tsv.TSV_ERR_ARG
+    assert fused(*walk, 1.0, 0, 8, 100, *[P] * 5, *[P] * 5, 2, 64, 16, 4, 8, 0, P, P) == tsv.TSV_OK
     # single-chunk plans need no workspace
     assert lib.tsv_attn_workspace_size(1, 15, 8, 2, 64, 16, 16, tsv.TSV_F32) == 0
     assert lib.tsv_attn_workspace_size(1, 15, 8, 2, 64, 16, 17, tsv.TSV_F32) > 0  # prefix may need 2 chunks
     assert lib.tsv_attn_workspace_size(1, 15, 8, 2, 96, 16, 17, tsv.TSV_F32) == 0
+
+
+def test_error_bits_match_the_header():
+    import re
+    text = open(tsv.HEADER if hasattr(tsv, "HEADER") else __import__("os").path.join(
+        __import__("os").path.dirname(__file__), "..", "include", "tsv.h")).read()
+    for name in ["TSV_DERR_PARENT", "TSV_DERR_BLOCK", "TSV_DERR_CAPACITY", "TSV_DERR_TOKEN", "TSV_DERR_NONFINITE",
+                 "TSV_DERR_TIMEOUT"]:
+        m = re.search(name + r"\s*=\s*(\d+)", text)
+        assert m and int(m.group(1)) == getattr(tsv, name), name

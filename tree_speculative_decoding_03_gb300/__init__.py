@@ -18,6 +18,8 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "tsv.h")
 
 TSV_OK, TSV_ERR_ARG, TSV_ERR_UNSUPPORTED, TSV_ERR_CUDA = 0, 1, 2, 3
 TSV_BF16, TSV_F32 = 0, 1
+# device-side data error bits in seq_err (include/tsv.h)
+TSV_DERR_PARENT, TSV_DERR_BLOCK, TSV_DERR_CAPACITY, TSV_DERR_TOKEN, TSV_DERR_NONFINITE, TSV_DERR_TIMEOUT = 1, 2, 4, 8, 16, 32
 DERR_PARENT, DERR_BLOCK, DERR_CAPACITY, DERR_TOKEN, DERR_NONFINITE = 1, 2, 4, 8, 16
 
 _lib = None
@@ -63,6 +65,9 @@ def load():
     lib.tsv_noalloc_scratch_bytes.argtypes = []
     lib.tsv_kv_compact_accepted.restype = i32
     lib.tsv_kv_compact_accepted.argtypes = [P] * 7 + [i32] * 8 + [P, P]
+    lib.tsv_tree_reject_sample_compact.restype = i32
+    lib.tsv_tree_reject_sample_compact.argtypes = ([P, P, P, P, P, P, f32, i32, i32, i32, P, P, P, P, P] + [P] * 5 +
+                                                   [i32] * 6 + [P, P])
     _lib = lib
     return lib
 
@@ -145,6 +150,21 @@ def tree_reject_sample(target_logits, draft_probs, draft_tokens, parent, u_accep
         _ptr(target_logits), _ptr(draft_probs), _ptr(draft_tokens), _ptr(parent), _ptr(u_accept), _ptr(u_bonus),
         float(temperature), B, N, V, _ptr(accepted_nodes), _ptr(accept_len), _ptr(bonus_token), _ptr(out_tokens),
         _ptr(seq_err), _stream(stream)))
+
+
+def tree_reject_sample_compact(target_logits, draft_probs, draft_tokens, parent, u_accept, u_bonus,
+                               temperature: float, accepted_nodes, accept_len, bonus_token, out_tokens, seq_err,
+                               k_cache, v_cache, block_table, seq_lens, new_seq_lens, compact_err, stream=None):
+    """The walk and the KV-cache rewrite of its accepted path in one launch (see include/tsv.h)."""
+    _contig(target_logits, draft_probs, draft_tokens, parent, u_accept, u_bonus, accepted_nodes, accept_len,
+            bonus_token, out_tokens, seq_err, k_cache, v_cache, block_table, seq_lens, new_seq_lens, compact_err)
+    B, N, V = target_logits.shape
+    num_blocks, bs, Hkv, D = k_cache.shape
+    _check(load().tsv_tree_reject_sample_compact(
+        _ptr(target_logits), _ptr(draft_probs), _ptr(draft_tokens), _ptr(parent), _ptr(u_accept), _ptr(u_bonus),
+        float(temperature), B, N, V, _ptr(accepted_nodes), _ptr(accept_len), _ptr(bonus_token), _ptr(out_tokens),
+        _ptr(seq_err), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(new_seq_lens), Hkv, D,
+        bs, block_table.shape[1], num_blocks, _dtype_code(k_cache), _ptr(compact_err), _stream(stream)))
 
 
 def kv_compact_accepted(k_cache, v_cache, block_table, seq_lens, accepted_nodes, accept_len, new_seq_lens,

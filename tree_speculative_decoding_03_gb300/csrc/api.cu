@@ -164,39 +164,101 @@ tsv_status tsv_tree_verify_attn(const void* q, const void* k_cache, const void* 
     return TSV_OK;
 }
 
-tsv_status tsv_tree_reject_sample(const float* target_logits, const float* draft_probs,
-                                  const int32_t* draft_tokens, const int32_t* parent, const float* u_accept,
-                                  const float* u_bonus, float temperature, int B, int N, int V,
-                                  int32_t* accepted_nodes, int32_t* accept_len, int32_t* bonus_token,
-                                  int32_t* out_tokens, int32_t* seq_err, void* stream) {
+}  // extern "C"
+
+namespace {
+// Argument checks and packing shared by the walk alone and the walk with fused compaction.
+tsv_status reject_args(const float* target_logits, const float* draft_probs, const int32_t* draft_tokens,
+                       const int32_t* parent, const float* u_accept, const float* u_bonus, float temperature, int B,
+                       int N, int V, int32_t* accepted_nodes, int32_t* accept_len, int32_t* bonus_token,
+                       int32_t* out_tokens, int32_t* seq_err, tsv::SampleArgs* a) {
     if (B < 0 || N < 1 || V < 1) return fail(TSV_ERR_ARG, "bad sizes B=%d N=%d V=%d", B, N, V);
     if (N > tsv::kMaxNodes) return fail(TSV_ERR_UNSUPPORTED, "N=%d exceeds %d tree nodes", N, tsv::kMaxNodes);
     if (V > 16 * 512 * 32) return fail(TSV_ERR_UNSUPPORTED, "V=%d exceeds %d", V, 16 * 512 * 32);
     if (!(temperature >= 0.0f) || !isfinite(temperature)) return fail(TSV_ERR_ARG, "temperature must be finite and >= 0");
     if (temperature > 0.0f && temperature < 1e-6f)
         return fail(TSV_ERR_UNSUPPORTED, "temperature %g in (0, 1e-6): use 0 for greedy matching", temperature);
-    if (B == 0) return TSV_OK;
     const bool greedy = temperature == 0.0f;
-    if (!target_logits || !draft_tokens || !parent || !accepted_nodes || !accept_len || !bonus_token ||
-        !out_tokens || !seq_err || (!greedy && (!draft_probs || !u_accept || !u_bonus)))
+    if (B > 0 && (!target_logits || !draft_tokens || !parent || !accepted_nodes || !accept_len || !bonus_token ||
+                  !out_tokens || !seq_err || (!greedy && (!draft_probs || !u_accept || !u_bonus))))
         return fail(TSV_ERR_ARG, "null array argument");
-    tsv::SampleArgs a{};
-    a.logits = target_logits;
-    a.probs = greedy ? nullptr : draft_probs;
-    a.tokens = draft_tokens;
-    a.parent = parent;
-    a.u_accept = u_accept;
-    a.u_bonus = u_bonus;
-    a.T = temperature;
-    a.N = N;
-    a.V = V;
-    a.accepted_nodes = accepted_nodes;
-    a.accept_len = accept_len;
-    a.bonus_token = bonus_token;
-    a.out_tokens = out_tokens;
-    a.seq_err = seq_err;
+    *a = tsv::SampleArgs{};
+    a->logits = target_logits;
+    a->probs = greedy ? nullptr : draft_probs;
+    a->tokens = draft_tokens;
+    a->parent = parent;
+    a->u_accept = u_accept;
+    a->u_bonus = u_bonus;
+    a->T = temperature;
+    a->N = N;
+    a->V = V;
+    a->accepted_nodes = accepted_nodes;
+    a->accept_len = accept_len;
+    a->bonus_token = bonus_token;
+    a->out_tokens = out_tokens;
+    a->seq_err = seq_err;
+    return TSV_OK;
+}
+
+tsv_status compact_args(void* k_cache, void* v_cache, const int32_t* block_table, const int32_t* seq_lens,
+                        int32_t* new_seq_lens, int B, int N, int Hkv, int D, int block_size, int max_blocks,
+                        int num_blocks, tsv_dtype dtype, int32_t* seq_err) {
+    if (B < 0 || N < 1 || Hkv < 1 || max_blocks < 1 || num_blocks < 1)
+        return fail(TSV_ERR_ARG, "bad sizes B=%d N=%d Hkv=%d", B, N, Hkv);
+    if (N > tsv::kMaxNodes) return fail(TSV_ERR_UNSUPPORTED, "N=%d exceeds %d tree nodes", N, tsv::kMaxNodes);
+    if (D != 64 && D != 128) return fail(TSV_ERR_UNSUPPORTED, "head dim %d not in {64, 128}", D);
+    if (!pow2_in(block_size, 8, 128)) return fail(TSV_ERR_UNSUPPORTED, "block_size %d not a power of two in [8,128]", block_size);
+    if (dtype != TSV_BF16 && dtype != TSV_F32) return fail(TSV_ERR_ARG, "bad dtype %d", (int)dtype);
+    if (B > 0 && (!k_cache || !v_cache || !block_table || !seq_lens || !new_seq_lens || !seq_err))
+        return fail(TSV_ERR_ARG, "null array argument");
+    if (B > 0 && (!aligned16(k_cache) || !aligned16(v_cache))) return fail(TSV_ERR_ARG, "caches must be 16-byte aligned");
+    return TSV_OK;
+}
+}  // namespace
+
+extern "C" {
+
+tsv_status tsv_tree_reject_sample(const float* target_logits, const float* draft_probs,
+                                  const int32_t* draft_tokens, const int32_t* parent, const float* u_accept,
+                                  const float* u_bonus, float temperature, int B, int N, int V,
+                                  int32_t* accepted_nodes, int32_t* accept_len, int32_t* bonus_token,
+                                  int32_t* out_tokens, int32_t* seq_err, void* stream) {
+    tsv::SampleArgs a;
+    const tsv_status st = reject_args(target_logits, draft_probs, draft_tokens, parent, u_accept, u_bonus, temperature,
+                                      B, N, V, accepted_nodes, accept_len, bonus_token, out_tokens, seq_err, &a);
+    if (st != TSV_OK || B == 0) return st;
     cudaError_t e = tsv::launch_tree_reject(a, B, device_sms(), static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "tree_reject_sample launch");
+    return TSV_OK;
+}
+
+tsv_status tsv_tree_reject_sample_compact(const float* target_logits, const float* draft_probs,
+                                          const int32_t* draft_tokens, const int32_t* parent, const float* u_accept,
+                                          const float* u_bonus, float temperature, int B, int N, int V,
+                                          int32_t* accepted_nodes, int32_t* accept_len, int32_t* bonus_token,
+                                          int32_t* out_tokens, int32_t* seq_err, void* k_cache, void* v_cache,
+                                          const int32_t* block_table, const int32_t* seq_lens,
+                                          int32_t* new_seq_lens, int Hkv, int D, int block_size, int max_blocks,
+                                          int num_blocks, tsv_dtype dtype, int32_t* compact_err, void* stream) {
+    tsv::SampleArgs a;
+    tsv_status st = reject_args(target_logits, draft_probs, draft_tokens, parent, u_accept, u_bonus, temperature, B,
+                                N, V, accepted_nodes, accept_len, bonus_token, out_tokens, seq_err, &a);
+    if (st != TSV_OK) return st;
+    st = compact_args(k_cache, v_cache, block_table, seq_lens, new_seq_lens, B, N, Hkv, D, block_size, max_blocks,
+                      num_blocks, dtype, compact_err);
+    if (st != TSV_OK || B == 0) return st;
+    a.k_cache = static_cast<uint8_t*>(k_cache);
+    a.v_cache = static_cast<uint8_t*>(v_cache);
+    a.block_table = block_table;
+    a.seq_lens = seq_lens;
+    a.new_seq_lens = new_seq_lens;
+    a.compact_err = compact_err;
+    a.row_bytes = Hkv * D * (dtype == TSV_F32 ? 4 : 2);
+    a.bs_log2 = log2i(block_size);
+    a.max_blocks = max_blocks;
+    a.num_blocks = num_blocks;
+    cudaError_t e = tsv::launch_tree_reject(a, B, device_sms(), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tree_reject_sample_compact launch");
     return TSV_OK;
 }
 
@@ -205,17 +267,10 @@ tsv_status tsv_kv_compact_accepted(void* k_cache, void* v_cache, const int32_t* 
                                    const int32_t* accept_len, int32_t* new_seq_lens, int B, int N, int Hkv, int D,
                                    int block_size, int max_blocks, int num_blocks, tsv_dtype dtype,
                                    int32_t* seq_err, void* stream) {
-    if (B < 0 || N < 1 || Hkv < 1 || max_blocks < 1 || num_blocks < 1)
-        return fail(TSV_ERR_ARG, "bad sizes B=%d N=%d Hkv=%d", B, N, Hkv);
-    if (N > tsv::kMaxNodes) return fail(TSV_ERR_UNSUPPORTED, "N=%d exceeds %d tree nodes", N, tsv::kMaxNodes);
-    if (D != 64 && D != 128) return fail(TSV_ERR_UNSUPPORTED, "head dim %d not in {64, 128}", D);
-    if (!pow2_in(block_size, 8, 128)) return fail(TSV_ERR_UNSUPPORTED, "block_size %d not a power of two in [8,128]", block_size);
-    if (dtype != TSV_BF16 && dtype != TSV_F32) return fail(TSV_ERR_ARG, "bad dtype %d", (int)dtype);
-    if (B == 0) return TSV_OK;
-    if (!k_cache || !v_cache || !block_table || !seq_lens || !accepted_nodes || !accept_len || !new_seq_lens ||
-        !seq_err)
-        return fail(TSV_ERR_ARG, "null array argument");
-    if (!aligned16(k_cache) || !aligned16(v_cache)) return fail(TSV_ERR_ARG, "caches must be 16-byte aligned");
+    tsv_status st = compact_args(k_cache, v_cache, block_table, seq_lens, new_seq_lens, B, N, Hkv, D, block_size,
+                                 max_blocks, num_blocks, dtype, seq_err);
+    if (st != TSV_OK || B == 0) return st;
+    if (!accepted_nodes || !accept_len) return fail(TSV_ERR_ARG, "null array argument");
     cudaError_t e = tsv::launch_kv_compact(k_cache, v_cache, block_table, seq_lens, accepted_nodes, accept_len,
                                            new_seq_lens, B, N, Hkv, D, block_size, max_blocks, num_blocks,
                                            dtype == TSV_F32 ? 4 : 2, seq_err, static_cast<cudaStream_t>(stream));

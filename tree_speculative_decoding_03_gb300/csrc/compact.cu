@@ -5,14 +5,9 @@
 // "Issue: Speculative Decoding on vLLM": trees require this rewrite.  SGLang
 // "SpeculativeDecoding", prefix match: rejected tokens' KV is evicted.
 //
-// One CTA per sequence.  A slot holds Hkv*D elements contiguously in the
-// [num_blocks, block_size, Hkv, D] layout, so moving one path row is one
-// contiguous copy per cache, done with 16-byte vector loads/stores.  Path rows
-// are moved in increasing j with a barrier after each: the source of row j is
-// slot L + a_j with a_j >= j, so it can be the destination of a later row
-// (a_j == j' > j) but never of an earlier one -- copying in order, each row fully
-// read before the next is written, is the in-place safe order.
-#include "common.cuh"
+// One CTA per sequence; the rewrite itself is compact_path (compact_path.cuh), which
+// the verifier's fused tail runs too.
+#include "compact_path.cuh"
 
 namespace tsv {
 
@@ -35,55 +30,12 @@ __global__ void __launch_bounds__(256) kv_compact_kernel(
         }
         return;
     }
-    const int32_t* path = accepted_nodes + (long long)b * N;
-    int e = 0;
-    if (A > N - 1) {
-        e = TSV_DERR_PARENT;
-    } else {
-        if (threadIdx.x == 0) s_flag = 1;
-        __syncthreads();
-        for (int j = threadIdx.x; j <= A; j += blockDim.x) {
-            int a = path[j];
-            s_path[j] = a;
-            bool ok = (j == 0) ? (a == 0) : (a > path[j - 1] && a < N);
-            if (!ok) s_flag = 0;
-        }
-        __syncthreads();
-        if (!s_flag) e = TSV_DERR_PARENT;
-        __syncthreads();
-    }
-    const int32_t* bt = block_table + (long long)b * max_blocks;
-    if (!e) e = block_cache_errors(bt, L, N, 1 << bs_log2, max_blocks, num_blocks, &s_flag);
-    if (e) {
-        if (threadIdx.x == 0) {
-            seq_err[b] = e;
-            new_seq_lens[b] = L;
-        }
-        return;
-    }
-    const int nvec = row_bytes >> 4;
-    for (int j = 1; j <= A; ++j) {
-        const int a = s_path[j];
-        if (a != j) {
-            const long long src = phys_row(bt, L + a, bs_log2) * row_bytes;
-            const long long dst = phys_row(bt, L + j, bs_log2) * row_bytes;
-            const uint4* ks = reinterpret_cast<const uint4*>(k_cache + src);
-            const uint4* vs = reinterpret_cast<const uint4*>(v_cache + src);
-            uint4* kd = reinterpret_cast<uint4*>(k_cache + dst);
-            uint4* vd = reinterpret_cast<uint4*>(v_cache + dst);
-            for (int i = threadIdx.x; i < 2 * nvec; i += blockDim.x) {
-                if (i < nvec) {
-                    kd[i] = ks[i];
-                } else {
-                    vd[i - nvec] = vs[i - nvec];
-                }
-            }
-        }
-        __syncthreads();
-    }
+    const int e = compact_path(k_cache, v_cache, block_table + (long long)b * max_blocks, L, A,
+                               accepted_nodes + (long long)b * N, N, row_bytes, bs_log2, max_blocks, num_blocks,
+                               &s_flag, s_path);
     if (threadIdx.x == 0) {
-        new_seq_lens[b] = L + 1 + A;
-        seq_err[b] = 0;
+        seq_err[b] = e;
+        new_seq_lens[b] = e ? L : L + 1 + A;
     }
 }
 

@@ -39,7 +39,7 @@
 #include <map>
 #include <mutex>
 
-#include "common.cuh"
+#include "compact_path.cuh"
 #include "verify_args.cuh"
 
 namespace cg = cooperative_groups;
@@ -324,6 +324,22 @@ __device__ __forceinline__ void rebuild_level(float (&lv)[VEC][4], const float* 
             }
             lv[k][e] = (v < v1) ? p : 0.0f;
         }
+    }
+}
+
+// Fused tail (rank 0 of the cluster, every thread): the KV-cache rewrite of the
+// accepted path, exactly as the compaction kernel does it; A < 0 (walk error) leaves
+// the sequence untouched.
+__device__ __forceinline__ void fused_compact(const SampleArgs& a, int b, int A, const int* path, int* s_flag,
+                                              int* s_path) {
+    const int L = a.seq_lens[b];
+    int e = 0;
+    if (A >= 0)
+        e = compact_path(a.k_cache, a.v_cache, a.block_table + (long long)b * a.max_blocks, L, A, path, a.N,
+                         a.row_bytes, a.bs_log2, a.max_blocks, a.num_blocks, s_flag, s_path);
+    if (threadIdx.x == 0) {
+        a.compact_err[b] = e;
+        a.new_seq_lens[b] = (A < 0 || e) ? L : L + 1 + A;
     }
 }
 
@@ -733,6 +749,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
             }
         }
         cluster.sync();
+        if (a.k_cache && rank == 0) fused_compact(a, b, -1, s_path, &s_flag, s_path);
         return;
     }
     if (rank == 0) {
@@ -751,6 +768,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
             a.out_tokens[rowoff + plen - 1] = amax;
         }
         cluster.sync();
+        if (a.k_cache && rank == 0) fused_compact(a, b, plen - 1, s_path, &s_flag, s_path);
         return;
     }
 
@@ -883,6 +901,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
         }
     }
     cluster.sync();
+    if (a.k_cache && rank == 0) fused_compact(a, b, plen - 1, s_path, &s_flag, s_path);
 }
 
 }  // namespace tsv

@@ -22,6 +22,15 @@ struct SampleArgs {
     int32_t* bonus_token;
     int32_t* out_tokens;
     int32_t* seq_err;
+    // fused KV-cache rewrite of the accepted path (k_cache == nullptr: none); same
+    // arguments and results as the compaction kernel, errors in compact_err
+    uint8_t* k_cache;
+    uint8_t* v_cache;
+    const int32_t* block_table;
+    const int32_t* seq_lens;
+    int32_t* new_seq_lens;
+    int32_t* compact_err;
+    int row_bytes, bs_log2, max_blocks, num_blocks;
 };
 
 cudaError_t launch_tree_reject(SampleArgs a, int B, int num_sms, cudaStream_t stream);
