@@ -20,13 +20,28 @@ namespace tsv {
 
 constexpr int kCompactVecs = 8;  // 16-byte vectors one thread stages per chunk
 
+// The cache check of block_cache_errors by one warp, without block barriers (so it can
+// run while the rest of the block does other work): TSV_DERR_CAPACITY, TSV_DERR_BLOCK or 0.
+__device__ __forceinline__ int warp_cache_errors(const int32_t* bt_row, int L, int N, int bs, int max_blocks,
+                                                 int num_blocks) {
+    if ((long long)L < 0 || (long long)L + N > (long long)max_blocks * bs) return TSV_DERR_CAPACITY;
+    const int nblk = (L + N + bs - 1) / bs;
+    bool bad = false;
+    for (int j = (int)(threadIdx.x & 31); j < nblk; j += 32) {
+        const int id = bt_row[j];
+        bad |= id < 0 || id >= num_blocks;
+    }
+    return __any_sync(0xffffffffu, bad) ? TSV_DERR_BLOCK : 0;
+}
+
 // Checks the path 0 = a_0 < a_1 < ... < a_A < N (TSV_DERR_PARENT), then the cache
 // capacity and block ids of slots [0, L + N) (TSV_DERR_CAPACITY / TSV_DERR_BLOCK), and
 // moves the rows.  Returns the error (0: done).  Called by every thread of the block;
 // `path` may point to global or shared memory; s_flag and s_path are shared scratch.
+// block_err >= 0: the cache check was already made (its result); < 0: make it here.
 __device__ __forceinline__ int compact_path(uint8_t* k_cache, uint8_t* v_cache, const int32_t* bt, int L, int A,
                                             const int32_t* path, int N, int row_bytes, int bs_log2, int max_blocks,
-                                            int num_blocks, int* s_flag, int* s_path) {
+                                            int num_blocks, int* s_flag, int* s_path, int block_err = -1) {
     int e = 0;
     if (A > N - 1) {
         e = TSV_DERR_PARENT;
@@ -43,7 +58,7 @@ __device__ __forceinline__ int compact_path(uint8_t* k_cache, uint8_t* v_cache, 
         if (!*s_flag) e = TSV_DERR_PARENT;
         __syncthreads();
     }
-    if (!e) e = block_cache_errors(bt, L, N, 1 << bs_log2, max_blocks, num_blocks, s_flag);
+    if (!e) e = block_err >= 0 ? block_err : block_cache_errors(bt, L, N, 1 << bs_log2, max_blocks, num_blocks, s_flag);
     if (e) return e;
     // items (row j = 1..A, cache, vector) in increasing row order, a pass of them at a time:
     // a pass is read completely before any of it is written

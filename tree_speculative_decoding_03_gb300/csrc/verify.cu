@@ -331,12 +331,12 @@ __device__ __forceinline__ void rebuild_level(float (&lv)[VEC][4], const float* 
 // accepted path, exactly as the compaction kernel does it; A < 0 (walk error) leaves
 // the sequence untouched.
 __device__ __forceinline__ void fused_compact(const SampleArgs& a, int b, int A, const int* path, int* s_flag,
-                                              int* s_path) {
+                                              int* s_path, int block_err) {
     const int L = a.seq_lens[b];
     int e = 0;
     if (A >= 0)
         e = compact_path(a.k_cache, a.v_cache, a.block_table + (long long)b * a.max_blocks, L, A, path, a.N,
-                         a.row_bytes, a.bs_log2, a.max_blocks, a.num_blocks, s_flag, s_path);
+                         a.row_bytes, a.bs_log2, a.max_blocks, a.num_blocks, s_flag, s_path, block_err);
     if (threadIdx.x == 0) {
         a.compact_err[b] = e;
         a.new_seq_lens[b] = (A < 0 || e) ? L : L + 1 + A;
@@ -389,6 +389,15 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
     const ff invT_ff = greedy ? ff_make(0.0f) : ff_div(ff_make(1.0f), ff_make(T));
 
     int parity = 0;
+
+    // fused rewrite (rank 0): the last warp checks the sequence's cache blocks now, while
+    // the walk runs, so the tail only checks the path and moves the rows
+    __shared__ int s_blkerr;
+    if (a.k_cache != nullptr && rank == 0 && warp == nwarps - 1) {
+        const int e = warp_cache_errors(a.block_table + (long long)b * a.max_blocks, a.seq_lens[b], N,
+                                        1 << a.bs_log2, a.max_blocks, a.num_blocks);
+        if (lane == 0) s_blkerr = e;
+    }
 
     // ---- tree and tokens
     for (int i = tid; i < N; i += blockDim.x) {
@@ -749,7 +758,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
             }
         }
         cluster.sync();
-        if (a.k_cache && rank == 0) fused_compact(a, b, -1, s_path, &s_flag, s_path);
+        if (a.k_cache && rank == 0) fused_compact(a, b, -1, s_path, &s_flag, s_path, s_blkerr);
         return;
     }
     if (rank == 0) {
@@ -768,7 +777,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
             a.out_tokens[rowoff + plen - 1] = amax;
         }
         cluster.sync();
-        if (a.k_cache && rank == 0) fused_compact(a, b, plen - 1, s_path, &s_flag, s_path);
+        if (a.k_cache && rank == 0) fused_compact(a, b, plen - 1, s_path, &s_flag, s_path, s_blkerr);
         return;
     }
 
@@ -901,7 +910,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
         }
     }
     cluster.sync();
-    if (a.k_cache && rank == 0) fused_compact(a, b, plen - 1, s_path, &s_flag, s_path);
+    if (a.k_cache && rank == 0) fused_compact(a, b, plen - 1, s_path, &s_flag, s_path, s_blkerr);
 }
 
 }  // namespace tsv
