@@ -199,24 +199,33 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool b_mn_major)
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// key t of the work item's range is visible to a row whose root-to-node path is the
-// bit set anc: every prefix key (t < L) below the range end, and the tree key L + j iff
-// node j is on the path
-__device__ __forceinline__ bool key_visible(int t, int k_end, int L, uint32_t anc0, uint32_t anc1, uint32_t anc2,
-                                            uint32_t anc3) {
-    if (t >= k_end) return false;
-    if (t < L) return true;
-    const int jn = t - L;
-    const uint32_t w = jn < 64 ? (jn < 32 ? anc0 : anc1) : (jn < 96 ? anc2 : anc3);
-    return (w >> (jn & 31)) & 1u;
+// Visibility of 32 consecutive keys to a row whose root-to-node path is the bit set
+// anc (bits 0..N-1 only): bit c covers the key with tree index base + c, i.e. key
+// L + base + c.  Every prefix key (tree index < 0) is visible, and the tree key L + j
+// iff node j is on the path; keys past the last node have no bit in anc, so they are
+// hidden too.
+__device__ __forceinline__ uint32_t vis_word(int base, uint32_t anc0, uint32_t anc1, uint32_t anc2,
+                                             uint32_t anc3) {
+    if (base <= -32) return 0xffffffffu;
+    if (base >= 128) return 0u;
+    if (base < 0) return (0xffffffffu >> (32 + base)) | (anc0 << -base);
+    const int wi = base >> 5;
+    const uint32_t lo = wi == 0 ? anc0 : (wi == 1 ? anc1 : (wi == 2 ? anc2 : anc3));
+    const uint32_t hi = wi == 0 ? anc1 : (wi == 1 ? anc2 : (wi == 2 ? anc3 : 0u));
+    return __funnelshift_r(lo, hi, static_cast<uint32_t>(base & 31));
 }
 
-// byte offset of 16-byte chunk `q` (along the contiguous dimension) of row `row` in a
-// tile stored as 64-element halves of [128 rows x 128 B], 128B-swizzled
-__device__ __forceinline__ uint32_t sw128_offset(int row, int q) {
-    const int half = q >> 3, cc = q & 7;
-    return static_cast<uint32_t>(half * kHalfBytes + (row >> 3) * 1024 + (row & 7) * 128 + ((cc ^ (row & 7)) << 4));
+// 16-byte global -> shared copy completing asynchronously (zero-filled when !take)
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool take) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(take ? 16 : 0)
+                 : "memory");
 }
+__device__ __forceinline__ uint32_t opaque_u32(uint32_t x) {
+    uint32_t y;
+    asm volatile("mov.b32 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
@@ -644,30 +653,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         const long long T_all = reinterpret_cast<const long long*>(s_sched)[4];
         bool ok = true;
 
-        // Q rows of unit (bq, gq) -> this warpgroup's swizzled shared tile
-        auto load_q = [&](int bq, int gq) {
-            uint8_t* qt = smem + lay.q0 + wg * (128u * D * 2u);
+        // Q rows of unit (bq, gq) -> this warpgroup's shared tile, stored as 64-element
+        // halves of [128 rows x 128 B] with the 128B swizzle (16-byte chunk c of row r at
+        // chunk c ^ (r & 7)); the copies are issued by issue_q and become visible to the
+        // MMA issuer with finish_q
+        auto issue_q = [&](int bq, int gq) {
+            // the row's swizzle phase goes through an opaque move, so the chunk addresses
+            // are formed here instead of being kept in registers across the tile loop
+            const uint32_t r7 = opaque_u32(static_cast<uint32_t>(tw & 7));
+            const uint32_t dst = smem_u32(smem + lay.q0 + wg * (128u * D * 2u)) + (tw >> 3) * 1024u + r7 * 128u;
             const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
                                                               (((long long)bq * N + n) * a.Hq + gq * a.G + hj) * D);
 #pragma unroll
-            for (int qq = 0; qq < D / 8; ++qq) {
-                uint4 v = valid ? __ldg(src + qq) : make_uint4(0, 0, 0, 0);
-                *reinterpret_cast<uint4*>(qt + sw128_offset(tw, qq)) = v;
-            }
+            for (int qq = 0; qq < D / 8; ++qq)
+                cp_async16(dst + (qq >> 3) * kHalfBytes + (((qq & 7) ^ r7) << 4), src + qq, valid);
+        };
+        auto finish_q = [&]() {
+            cp_async_wait_all();
             fence_proxy_async_smem();
             mbar_arrive(bar(Bars::kQ));
         };
 
         TileIt it = it0;
         int jt = 0, seg = 0;
-        if (count > 0) load_q(it.b, it.g);
+        // parent of node stid in the coming segment's sequence (loaded one segment ahead)
+        int par_next = 0;
+        if (count > 0) {
+            issue_q(it.b, it.g);
+            if (stid < N) par_next = __ldg(a.parent + (long long)it.b * N + stid);
+            finish_q();
+        }
         while (jt < count) {
             // ---- segment: tiles [t_first, t_first + ntl) of unit (b, g)
             const int b = it.b, g = it.g, L = it.L, Tb = it.Tb, t_first = it.t;
             const int ntl = min(Tb - t_first, count - jt);
-            const int k_end = L + N;
             const bool whole = (t_first == 0) && (ntl == Tb);
             const long long unit_first = s_first + jt - t_first;  // global index of the unit's tile 0
+            const int par_cur = par_next;
+            // the Q rows and parents of the next segment's unit are fetched during this
+            // segment's last tile, once that tile's S product (the last reader of Q) is done
+            const bool more = jt + ntl < count;
             err_b = b;
             if (t_first == 0 && stid == 0) {
                 // this lane holds the unit's first piece: record where its pieces are
@@ -682,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t anc0 = 0u, anc1 = 0u, anc2 = 0u, anc3 = 0u;
             if ((long long)(t_first + ntl) * kTileKeys > L) {
                 int8_t* par = s_par + (seg & 1) * 128;
-                for (int i = stid; i < N; i += nthr) par[i] = static_cast<int8_t>(a.parent[(long long)b * N + i]);
+                if (stid < N) par[stid] = static_cast<int8_t>(par_cur);  // N <= 128 <= softmax threads
                 named_bar_sync(1, nthr);
                 if (valid) {
                     int x = n;
@@ -712,13 +737,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     continue;
                 }
                 tc_fence_after();
+                const bool last_of_seg = (i == ntl - 1);
+                if (last_of_seg && more) {
+                    TileIt nx = it;
+                    nx.next_unit(a);
+                    issue_q(nx.b, nx.g);
+                    if (stid < N) par_next = __ldg(a.parent + (long long)nx.b * N + stid);
+                }
                 if (warp_active) {
                     // Two passes over the S row in TMEM, 64 columns per wait: the raw max
                     // first, then P = 2^(s*scale - m) written as bf16 pairs over the S
                     // columns.  Independent accumulators (8 for the max, 4 for the sum) keep
-                    // the FMNMX/MUFU latency chains short; the masked path is taken only for
-                    // tiles that reach past the prefix.
+                    // the FMNMX/MUFU latency chains short.  A tile that reaches past the
+                    // prefix first sets its hidden scores to -inf (one visibility bit per
+                    // key) and stores them back, so both passes run the same code for
+                    // every tile.
                     const bool full_tile = (t0 + kTileKeys <= L);
+                    uint32_t vis0 = 0xffffffffu, vis1 = 0xffffffffu, vis2 = 0xffffffffu, vis3 = 0xffffffffu;
+                    if (!full_tile) {
+                        vis0 = vis_word(t0 - L, anc0, anc1, anc2, anc3);
+                        vis1 = vis_word(t0 + 32 - L, anc0, anc1, anc2, anc3);
+                        vis2 = vis_word(t0 + 64 - L, anc0, anc1, anc2, anc3);
+                        vis3 = vis_word(t0 + 96 - L, anc0, anc1, anc2, anc3);
+                    }
                     float mxa[8];
 #pragma unroll
                     for (int q = 0; q < 8; ++q) mxa[q] = -INFINITY;
@@ -728,22 +769,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_ld32(tS + h2 * 64, pa);
                         tmem_ld32(tS + h2 * 64 + 32, pb);
                         tmem_wait_ld();
+                        if (!full_tile) {
+                            const uint32_t va = h2 ? vis2 : vis0, vb = h2 ? vis3 : vis1;
+#pragma unroll
+                            for (int cc = 0; cc < 32; ++cc) {
+                                pa[cc] = ((va >> cc) & 1u) ? pa[cc] : 0xff800000u;  // -inf
+                                pb[cc] = ((vb >> cc) & 1u) ? pb[cc] : 0xff800000u;
+                            }
+                            tmem_st32(tS + h2 * 64, pa);
+                            tmem_st32(tS + h2 * 64 + 32, pb);
+                            tmem_wait_st();
+                        }
                         if (valid) {
-                            if (full_tile) {
 #pragma unroll
-                                for (int cc = 0; cc < 32; ++cc) {
-                                    mxa[cc & 7] = fmaxf(mxa[cc & 7], __uint_as_float(pa[cc]));
-                                    mxa[cc & 7] = fmaxf(mxa[cc & 7], __uint_as_float(pb[cc]));
-                                }
-                            } else {
-#pragma unroll
-                                for (int cc = 0; cc < 32; ++cc) {
-                                    const int c0 = h2 * 64 + cc;
-                                    if (key_visible(t0 + c0, k_end, L, anc0, anc1, anc2, anc3))
-                                        mxa[cc & 7] = fmaxf(mxa[cc & 7], __uint_as_float(pa[cc]));
-                                    if (key_visible(t0 + c0 + 32, k_end, L, anc0, anc1, anc2, anc3))
-                                        mxa[cc & 7] = fmaxf(mxa[cc & 7], __uint_as_float(pb[cc]));
-                                }
+                            for (int cc = 0; cc < 32; ++cc) {
+                                mxa[cc & 7] = fmaxf(mxa[cc & 7], __uint_as_float(pa[cc]));
+                                mxa[cc & 7] = fmaxf(mxa[cc & 7], __uint_as_float(pb[cc]));
                             }
                         }
                     }
@@ -788,23 +829,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_ld32(tS + h2 * 64, pa);
                         tmem_ld32(tS + h2 * 64 + 32, pb);
                         tmem_wait_ld();
-                        // P in place of the scores (as bit patterns): pa = columns 0..31, pb = 32..63
-                        if (live && full_tile) {
+                        // P in place of the scores (as bit patterns): pa = columns 0..31, pb =
+                        // 32..63; a hidden key's -inf score gives 2^-inf = 0
+                        if (live) {
 #pragma unroll
                             for (int cc = 0; cc < 32; ++cc) {
                                 pa[cc] = __float_as_uint(ex2(fmaf(__uint_as_float(pa[cc]), sl2, neg_m)));
                                 pb[cc] = __float_as_uint(ex2(fmaf(__uint_as_float(pb[cc]), sl2, neg_m)));
-                            }
-                        } else if (live) {
-#pragma unroll
-                            for (int cc = 0; cc < 32; ++cc) {
-                                const int c0 = h2 * 64 + cc;
-                                pa[cc] = key_visible(t0 + c0, k_end, L, anc0, anc1, anc2, anc3)
-                                             ? __float_as_uint(ex2(fmaf(__uint_as_float(pa[cc]), sl2, neg_m)))
-                                             : 0u;
-                                pb[cc] = key_visible(t0 + c0 + 32, k_end, L, anc0, anc1, anc2, anc3)
-                                             ? __float_as_uint(ex2(fmaf(__uint_as_float(pb[cc]), sl2, neg_m)))
-                                             : 0u;
                             }
                         } else {
 #pragma unroll
@@ -827,30 +858,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 // a unit's last tile: V rows past the key range are zeroed before the PV
                 // product (they may hold stale or foreign data; P is 0 there but 0 * NaN is NaN)
-                if (wg == 0 && k_end - t0 < kTileKeys) {
+                if (wg == 0 && L + N - t0 < kTileKeys) {
                     const int fV = 2 * jt + 1;
                     ok = ok && mbar_wait(bar(Bars::kFull + fV % nslots), (fV / nslots) & 1, s_abort);
                     if (ok) {
-                        uint8_t* vt = smem + lay.ring + (fV % nslots) * SLOT;
-                        const int row0 = k_end - t0;
-                        for (int idx = tw; idx < (kTileKeys - row0) * HALVES * 8; idx += 128) {
-                            const int per_half = (kTileKeys - row0) * 8;
-                            const int hh = idx / per_half, rem = idx % per_half;
-                            const int row = row0 + rem / 8, cq = rem % 8;
-                            *reinterpret_cast<uint4*>(vt + hh * kHalfBytes + row * 128 + cq * 16) = make_uint4(0, 0, 0, 0);
-                        }
+                        // rows [L + N - t0, 128) of both halves; a row is HALVES * 8 chunks of 16 B
+                        constexpr int kRowChunks = HALVES * 8, kRowsPerStep = 128 / kRowChunks;
+                        uint8_t* vt = smem + lay.ring + (fV % nslots) * SLOT + ((tw % kRowChunks) >> 3) * kHalfBytes +
+                                      (tw & 7) * 16;
+                        for (int row = L + N - t0 + tw / kRowChunks; row < kTileKeys; row += kRowsPerStep)
+                            *reinterpret_cast<uint4*>(vt + row * 128) = make_uint4(0, 0, 0, 0);
                     }
                 }
                 fence_proxy_async_smem();  // the zeroed V rows, written through the generic proxy
                 tc_fence_before();
                 mbar_arrive(bar(Bars::kP + sb));
                 if (!ok) *s_abort = 1;
-            }
-            // ---- next segment's Q: every S product of this segment has been read
-            TileIt nx = it;
-            if (jt < count) {
-                nx.next_unit(a);
-                load_q(nx.b, nx.g);
+                if (last_of_seg && more) finish_q();  // the next segment's Q rows are in place
             }
             // ---- epilogue: O / l of this segment
             if (ok) {
@@ -898,7 +922,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     a.part_l[prow] = l_run;
                 }
             }
-            it = nx;
+            if (more) it.next_unit(a);
             ++seg;
         }
         if (!ok) my_err = 1;
