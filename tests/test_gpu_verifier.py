@@ -76,6 +76,35 @@ def test_p_equals_q_full_accept_and_errors():
     _check(inp)
 
 
+@pytest.mark.parametrize("T", [0.0, 0.6, 1.0])
+@pytest.mark.parametrize("V", [3001, 32000])
+@pytest.mark.parametrize("N,tree", [(1, "chain"), (2, "chain"), (6, "chain"), (8, "random")])
+def test_small_trees(T, V, N, tree):
+    """Small trees down to the root alone and one-child chains, unaligned and aligned
+    vocabularies: decisions identical to the oracle's walk."""
+    w = W.CONFIGS[3].replace(B=64, Hq=4, Hkv=1, D=64, prefix=(0, 0), N=N, depth=4, tree=tree, V=V, T=T,
+                             seed=V + 10 * N + int(10 * T))
+    _check(W.generate(w, temperature=T))
+
+
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_small_tree_errors_only_on_visited_rows(T):
+    """A non-finite logit is an error only in a row the walk visits."""
+    w = W.CONFIGS[1].replace(B=8, Hq=4, Hkv=1, D=64, prefix=(0, 0), V=5000, seed=21)
+    inp = W.generate(w, temperature=T)
+    inp["target_logits"] = (np.log(inp["draft_probs"].astype(np.float64))).astype(np.float32)
+    inp["u_accept"] = (inp["u_accept"] * 0.999).astype(np.float32)
+    inp["draft_tokens"] = inp["draft_tokens"].copy()
+    inp["draft_tokens"][1, 3] = 5000                   # token out of range
+    inp["target_logits"][2, 0, 7] = np.inf             # root row: always visited
+    inp["target_logits"][3, 4, 11] = np.nan            # node 4: visited at T = 1 (p == q accepts)
+    inp["target_logits"][5, 0, inp["draft_tokens"][5, 1]] = -60.0  # child 1 rejected at the root ...
+    inp["target_logits"][5, 3, 11] = np.inf            # ... so node 3's row is never visited
+    g, o = _check(inp, T)
+    assert o["err"][5] == 0 and g["err"][5] == 0
+    assert o["err"][2] != 0
+
+
 def _markov(n, parent, V, T, rng, tgt, drf, x0):
     N = len(parent)
     kids = [[] for _ in range(N)]

@@ -104,12 +104,20 @@ __device__ __forceinline__ void fence_barrier_init() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// L2 policy for data read once: its lines are the first to be evicted, so the stream of
+// K/V tiles does not push out the code, Q rows, parents and block tables that every CTA
+// reads at its unit boundaries (measured: 1 - 3 % less time per launch)
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
-                                            int c2) {
+                                            int c2, uint64_t policy) {
     asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
-        "[%2];" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%3, "
+        "%4, %5}], [%2], %6;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
         : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
@@ -459,6 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // block ids are loaded while the current tile's fills wait for their slots.
         TileIt it = it0;
         int blk = (count > 0 && lane < 16) ? s_blk0[lane] : 0;  // looked up during set-up
+        const uint64_t kv_policy = l2_evict_first_policy();  // every K/V row is read once
         int seg = 0;
         for (int jt = 0; jt < count && !my_err; ++jt) {
             if (jt > 0 && it.t == 0) ++seg;
@@ -493,7 +502,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int hh = 0; hh < HALVES; ++hh)
                         tma_load_3d(dst + hh * kHalfBytes + lane * bs * 128, map, bar(Bars::kFull + slot), hh * 64, g,
-                                    blk_cur * bs);
+                                    blk_cur * bs, kv_policy);
                 }
             }
             if (jt == 0 && count > 1 && count <= kFirstTileAloneMaxTiles && !my_err &&
