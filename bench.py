@@ -54,8 +54,12 @@ def _peaks():
 
 
 def _source_digest():
+    """Digest of the GPU kernel sources (CUDA translation units and their headers):
+    the DRAM counters in profiles/traffic.json hold only for the kernels they were
+    taken on.  Host-only C++ (tree construction) does not enter."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "tree_speculative_decoding_03_gb300", "csrc", "*"))):
+    csrc = os.path.join(ROOT, "tree_speculative_decoding_03_gb300", "csrc")
+    for p in sorted(glob.glob(os.path.join(csrc, "*.cu")) + glob.glob(os.path.join(csrc, "*.cuh"))):
         with open(p, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]

@@ -208,6 +208,49 @@ tsv_status tsv_tree_reject_sample_compact(const float *target_logits, const floa
                                           int D, int block_size, int max_blocks, int num_blocks,
                                           tsv_dtype dtype, int32_t *compact_err, void *stream);
 
+/* ---------------------------------------------------------------------------
+ * Tree construction (host side).  Sequoia summary, sections "Scalable Speculative
+ * Decoding" and "Dynamic Programming": the tree of speculated tokens is built by
+ * dynamic programming to an optimal shape; the figure of forward-pass time against
+ * input length: the tree size trades the draft model's time against the target's
+ * verification time (hardware-aware).  The pages state neither the objective nor the
+ * recurrence; this library reads them as follows.
+ *
+ * accept[k], k = 0 .. K-1: probability that the (k+1)-th drafted sibling is the one
+ * the walk accepts at a node it has reached (positional acceptance, the same at every
+ * node; accept[k] >= 0, sum <= 1 + 1e-9); siblings of rank > K are never accepted.
+ * A node is reached with the product of accept[rank - 1] over the edges of its root
+ * path (rank = 1 + the number of earlier siblings), so the expected number of tokens
+ * a verification step generates -- accepted drafts plus the bonus -- is
+ *     E(tree) = sum over the tree's nodes of that product   (the root counts 1).
+ *
+ * These calls read and write HOST memory, run synchronously on the calling thread,
+ * need no GPU, and use O(min(d_max, n_max) * min(K, n_max) * n_max) bytes of
+ * temporary host memory.  Argument errors return TSV_ERR_ARG.
+ * ------------------------------------------------------------------------- */
+
+/* values[n * (d_max + 1) + d] = the largest E over trees of n nodes (root included)
+ * and depth <= d (root at depth 0), for 1 <= n <= n_max, 0 <= d <= d_max; row n = 0
+ * is 0, and -INFINITY where no tree exists (n > 1 with d = 0).
+ * 1 <= n_max <= 128, d_max >= 0, K >= 1; values holds (n_max + 1) * (d_max + 1). */
+tsv_status tsv_sequoia_values(const double *accept, int K, int n_max, int d_max, double *values);
+
+/* One tree of n nodes and depth <= max_depth attaining the largest E: parent[0..n-1]
+ * in breadth-first order with siblings by rank (parent[0] = -1, parent[i] < i, a
+ * node's children have increasing indices in draft order, the order in which the walk
+ * tries them); *expected = its E.  1 <= n <= 128; max_depth >= 1 unless n == 1. */
+tsv_status tsv_sequoia_tree(const double *accept, int K, int n, int max_depth, int32_t *parent,
+                            double *expected);
+
+/* Hardware-aware size and depth: the (n, d) with 1 <= n <= n_max, 0 <= d <= d_max that
+ * maximises  speedup(n, d) = E_best(n, d) * t_verify[1] / (t_verify[n] + d * t_draft),
+ * where t_verify[n] > 0 is the time of one target forward over n tree tokens
+ * (t_verify[1]: one incremental decoding step; t_verify[0] is not read) and
+ * t_draft >= 0 the time of one draft forward, run once per tree level.  Ties go to
+ * the smaller n, then the smaller d. */
+tsv_status tsv_sequoia_plan(const double *accept, int K, int n_max, int d_max, const double *t_verify,
+                            double t_draft, int *n_best, int *d_best, double *speedup);
+
 #ifdef __cplusplus
 }
 #endif

@@ -68,6 +68,13 @@ def load():
     lib.tsv_tree_reject_sample_compact.restype = i32
     lib.tsv_tree_reject_sample_compact.argtypes = ([P, P, P, P, P, P, f32, i32, i32, i32, P, P, P, P, P] + [P] * 5 +
                                                    [i32] * 6 + [P, P])
+    f64 = ctypes.c_double
+    lib.tsv_sequoia_values.restype = i32
+    lib.tsv_sequoia_values.argtypes = [P, i32, i32, i32, P]
+    lib.tsv_sequoia_tree.restype = i32
+    lib.tsv_sequoia_tree.argtypes = [P, i32, i32, i32, P, P]
+    lib.tsv_sequoia_plan.restype = i32
+    lib.tsv_sequoia_plan.argtypes = [P, i32, i32, i32, P, f64, P, P, P]
     _lib = lib
     return lib
 
@@ -177,3 +184,45 @@ def kv_compact_accepted(k_cache, v_cache, block_table, seq_lens, accepted_nodes,
         _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(accepted_nodes), _ptr(accept_len),
         _ptr(new_seq_lens), B, N, Hkv, D, bs, block_table.shape[1], num_blocks, _dtype_code(k_cache),
         _ptr(seq_err), _stream(stream)))
+
+
+# ----------------------------------------------------------------------------- tree construction
+# Host-side calls (numpy arrays, no GPU): the draft-tree shape with the largest expected
+# number of generated tokens per step, and the hardware-aware choice of size and depth
+# (see include/tsv.h for the acceptance model).
+
+def _f64(a):
+    import numpy as np
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def sequoia_values(accept, n_max: int, d_max: int):
+    """[n_max + 1, d_max + 1] array: best expected tokens per step of an n-node tree of
+    depth <= d (-inf where no tree exists)."""
+    import numpy as np
+    acc = _f64(accept)
+    out = np.empty((n_max + 1, d_max + 1), np.float64)
+    _check(load().tsv_sequoia_values(acc.ctypes.data, len(acc), n_max, d_max, out.ctypes.data))
+    return out
+
+
+def sequoia_tree(accept, n: int, max_depth: int):
+    """(parent[n] int32 in breadth-first order with siblings by rank, expected tokens)."""
+    import numpy as np
+    acc = _f64(accept)
+    parent = np.empty(n, np.int32)
+    e = ctypes.c_double()
+    _check(load().tsv_sequoia_tree(acc.ctypes.data, len(acc), n, max_depth, parent.ctypes.data, ctypes.byref(e)))
+    return parent, e.value
+
+
+def sequoia_plan(accept, n_max: int, d_max: int, t_verify, t_draft: float):
+    """(n, d, speedup) maximising E_best(n, d) * t_verify[1] / (t_verify[n] + d * t_draft);
+    t_verify[n] for n = 0..n_max (entry 0 is not read)."""
+    acc, tv = _f64(accept), _f64(t_verify)
+    if len(tv) < n_max + 1:
+        raise ValueError("t_verify needs n_max + 1 entries")
+    nb, db, sp = ctypes.c_int(), ctypes.c_int(), ctypes.c_double()
+    _check(load().tsv_sequoia_plan(acc.ctypes.data, len(acc), n_max, d_max, tv.ctypes.data, float(t_draft),
+                                   ctypes.byref(nb), ctypes.byref(db), ctypes.byref(sp)))
+    return nb.value, db.value, sp.value
