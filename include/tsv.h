@@ -251,6 +251,19 @@ tsv_status tsv_sequoia_tree(const double *accept, int K, int n, int max_depth, i
 tsv_status tsv_sequoia_plan(const double *accept, int K, int n_max, int d_max, const double *t_verify,
                             double t_draft, int *n_best, int *d_best, double *speedup);
 
+/* Acceptance statistics for the planner, accumulated from verification outputs (HOST
+ * copies of parent, accepted_nodes and accept_len, layouts as above).  For every
+ * sequence with accept_len[b] >= 0 and every node on its accepted path
+ * accepted_nodes[b, 0 .. accept_len[b]] -- the nodes the walk reached -- with c
+ * children: reached[k] += 1 for every rank k + 1 <= min(c, K), and accepted[r - 1] += 1
+ * when the path goes on to the child of rank r <= K.  Under the positional model above,
+ * accepted[k] / reached[k] estimates accept[k].  The counts are added to the arrays
+ * (int64 [K]), so steps can be accumulated; sequences with accept_len < 0 are skipped.
+ * TSV_ERR_ARG for a parent array that is not a tree or a path that does not follow it. */
+tsv_status tsv_sequoia_accept_counts(const int32_t *parent, const int32_t *accepted_nodes,
+                                     const int32_t *accept_len, int B, int N, int K, int64_t *reached,
+                                     int64_t *accepted);
+
 #ifdef __cplusplus
 }
 #endif

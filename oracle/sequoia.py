@@ -27,7 +27,10 @@ Functions, and what pins them (tests/test_oracle_sequoia.py):
   best_value_brute  max of tree_value over ordered_trees: the definition of E_best;
   dp_values       the recurrence, stated plainly; pinned to best_value_brute for every
                   n <= 9 and to closed forms at larger n;
-  plan            argmax of the speedup over the dp values, by its definition.
+  plan            argmax of the speedup over the dp values, by its definition;
+  accept_counts   the positional acceptance counts of walk outputs, by their
+                  definition; pinned by recovering a known acceptance vector from
+                  simulated walks.
 """
 from __future__ import annotations
 
@@ -179,3 +182,52 @@ def simulate_walk(parent: Sequence[int], accept: Sequence[float], trials: int, r
         node[idx[moved]] = nxt[moved]
         alive[idx[~moved]] = False
     return out
+
+
+def accept_counts(parent, accepted_nodes, accept_len, K: int):
+    """For every reached node (on an accepted path) with c children: reached[k] += 1 for
+    ranks k + 1 <= min(c, K); accepted[r - 1] += 1 when the path goes on to the child of
+    rank r <= K.  Sequences with accept_len < 0 are skipped."""
+    reached = np.zeros(K, np.int64)
+    accepted = np.zeros(K, np.int64)
+    for b in range(len(accept_len)):
+        A = int(accept_len[b])
+        if A < 0:
+            continue
+        par = [int(x) for x in parent[b]]
+        kids = [[] for _ in par]
+        for c in range(1, len(par)):
+            kids[par[c]].append(c)
+        path = [int(x) for x in accepted_nodes[b][:A + 1]]
+        for j, v in enumerate(path):
+            for k in range(min(len(kids[v]), K)):
+                reached[k] += 1
+            if j < A:
+                r = kids[v].index(path[j + 1]) + 1
+                if r <= K:
+                    accepted[r - 1] += 1
+    return reached, accepted
+
+
+def simulate_paths(parent, accept: Sequence[float], trials: int, rng: np.random.Generator):
+    """Accepted paths (accepted_nodes rows padded with -1, accept_len) of `trials` walks
+    on one tree under the positional model, for the estimator's pin."""
+    n = len(parent)
+    kids: List[List[int]] = [[] for _ in range(n)]
+    for v in range(1, n):
+        kids[int(parent[v])].append(v)
+    probs = np.append(np.asarray(accept, np.float64), max(0.0, 1.0 - float(np.sum(accept))))
+    probs = probs / probs.sum()
+    nodes = np.full((trials, n), -1, np.int32)
+    lens = np.zeros(trials, np.int32)
+    for t in range(trials):
+        v, path = 0, [0]
+        while True:
+            r = int(rng.choice(len(probs), p=probs)) + 1
+            if r > len(accept) or r > len(kids[v]):
+                break
+            v = kids[v][r - 1]
+            path.append(v)
+        nodes[t, :len(path)] = path
+        lens[t] = len(path) - 1
+    return nodes, lens

@@ -89,3 +89,17 @@ def test_plan_by_definition():
     n, d, _ = sq.plan(acc, 16, 6, [0.0] + [1.0] * 16, 0.0)
     F = sq.dp_values(acc, 16, 6)
     assert n == 16 and F[16, d] == F[16].max() and np.all(F[16, :d] < F[16, d])
+
+
+def test_accept_counts_recover_the_acceptance_vector():
+    # walks simulated under a known positional model on a tree where every rank up to 4
+    # occurs: accepted / reached estimates accept[k] (binomial, 5 sigma)
+    acc = [0.45, 0.2, 0.1, 0.05]
+    parent = [-1, 0, 0, 0, 0, 1, 1, 1, 1, 2, 2, 2, 5, 5, 5, 5]
+    rng = np.random.default_rng(7)
+    nodes, lens = sq.simulate_paths(parent, acc, 15_000, rng)
+    reached, accepted = sq.accept_counts([parent] * len(lens), nodes, lens, 4)
+    for k in range(4):
+        p_hat = accepted[k] / reached[k]
+        sigma = np.sqrt(acc[k] * (1 - acc[k]) / reached[k])
+        assert abs(p_hat - acc[k]) < 5 * sigma, (k, p_hat, acc[k])

@@ -105,3 +105,43 @@ def test_largest_problem_runs_in_well_under_a_second():
     dt = time.perf_counter() - t0
     print(f"tree construction, n_max 128, depth 127, 127 ranks: {dt * 1e3:.1f} ms")
     assert np.all(np.isfinite(v[1:, 1:])) and dt < 5.0
+
+
+def test_accept_counts_hand_case():
+    # root has children 1, 2 (ranks 1, 2); node 1 has 3, 4; node 2 has 5.  Path 0 -> 2 -> 5.
+    parent = np.array([[-1, 0, 0, 1, 1, 2]], np.int32)
+    nodes = np.array([[0, 2, 5, -1, -1, -1]], np.int32)
+    reached, accepted = tsv.sequoia_accept_counts(parent, nodes, np.array([2], np.int32), K=2)
+    assert list(reached) == [2, 1] and list(accepted) == [1, 1]
+    assert [list(x) for x in sq.accept_counts(parent, nodes, [2], 2)] == [[2, 1], [1, 1]]
+
+
+def test_accept_counts_match_oracle_on_walk_outputs():
+    import oracle
+    import workloads as W
+    w = W.CONFIGS[3].replace(B=48, Hq=4, Hkv=1, D=64, prefix=(0, 0), N=40, depth=6, V=800, T=1.0, seed=17)
+    inp = W.generate(w)
+    o = oracle.tree_reject_sample(inp)
+    inp2 = dict(inp)
+    inp2["parent"] = inp["parent"].copy()
+    inp2["parent"][3, 5] = 7  # a bad tree: the walk flags it (accept_len -1) and the counts skip it
+    o2 = oracle.tree_reject_sample(inp2)
+    assert o2["accept_len"][3] == -1
+    for K in (1, 4, 12):
+        r, a = tsv.sequoia_accept_counts(inp["parent"], o["accepted_nodes"], o["accept_len"], K)
+        r0, a0 = sq.accept_counts(inp["parent"], o["accepted_nodes"], o["accept_len"], K)
+        assert np.array_equal(r, r0) and np.array_equal(a, a0) and r.sum() > 0
+        # accumulation over two steps
+        r2, a2 = tsv.sequoia_accept_counts(inp2["parent"], o2["accepted_nodes"], o2["accept_len"], K,
+                                           reached=r.copy(), accepted=a.copy())
+        r1, a1 = sq.accept_counts(inp2["parent"], o2["accepted_nodes"], o2["accept_len"], K)
+        assert np.array_equal(r2, r + r1) and np.array_equal(a2, a + a1)
+
+
+def test_accept_counts_reject_inconsistent_inputs():
+    parent = np.array([[-1, 0, 0, 1]], np.int32)
+    with pytest.raises(tsv.TsvError):  # 3 is not a child of 2
+        tsv.sequoia_accept_counts(parent, np.array([[0, 2, 3, -1]], np.int32), np.array([2], np.int32), 2)
+    with pytest.raises(tsv.TsvError):  # parent[2] = 2 is not a tree
+        tsv.sequoia_accept_counts(np.array([[-1, 0, 2, 1]], np.int32), np.array([[0, 1, -1, -1]], np.int32),
+                                  np.array([1], np.int32), 2)

@@ -75,6 +75,8 @@ def load():
     lib.tsv_sequoia_tree.argtypes = [P, i32, i32, i32, P, P]
     lib.tsv_sequoia_plan.restype = i32
     lib.tsv_sequoia_plan.argtypes = [P, i32, i32, i32, P, f64, P, P, P]
+    lib.tsv_sequoia_accept_counts.restype = i32
+    lib.tsv_sequoia_accept_counts.argtypes = [P, P, P, i32, i32, i32, P, P]
     _lib = lib
     return lib
 
@@ -226,3 +228,24 @@ def sequoia_plan(accept, n_max: int, d_max: int, t_verify, t_draft: float):
     _check(load().tsv_sequoia_plan(acc.ctypes.data, len(acc), n_max, d_max, tv.ctypes.data, float(t_draft),
                                    ctypes.byref(nb), ctypes.byref(db), ctypes.byref(sp)))
     return nb.value, db.value, sp.value
+
+
+def sequoia_accept_counts(parent, accepted_nodes, accept_len, K: int, reached=None, accepted=None):
+    """Adds the positional acceptance counts of one step's walk outputs (host arrays) to
+    `reached` / `accepted` (int64 [K], new zero arrays if None) and returns them;
+    accepted / reached estimates the acceptance vector the planner takes."""
+    import numpy as np
+    par = np.ascontiguousarray(parent, np.int32)
+    nodes = np.ascontiguousarray(accepted_nodes, np.int32)
+    lens = np.ascontiguousarray(accept_len, np.int32)
+    B, N = par.shape
+    if nodes.shape != (B, N) or lens.shape != (B,):
+        raise ValueError("accepted_nodes must be [B, N] and accept_len [B] like parent")
+    reached = np.zeros(K, np.int64) if reached is None else reached
+    accepted = np.zeros(K, np.int64) if accepted is None else accepted
+    for a in (reached, accepted):
+        if a.dtype != np.int64 or a.shape != (K,) or not a.flags.c_contiguous:
+            raise ValueError("count arrays must be contiguous int64 [K]")
+    _check(load().tsv_sequoia_accept_counts(par.ctypes.data, nodes.ctypes.data, lens.ctypes.data, B, N, K,
+                                            reached.ctypes.data, accepted.ctypes.data))
+    return reached, accepted

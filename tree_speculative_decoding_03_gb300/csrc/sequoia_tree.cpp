@@ -8,6 +8,9 @@
 // trades draft time against verification time.  The objective and the recurrence are
 // not on the pages; the reading used here (positional acceptance vector, E(tree) =
 // sum over nodes of the probability that the walk reaches them) is stated in tsv.h.
+// The acceptance vector itself is estimated from verification outputs by
+// tsv_sequoia_accept_counts (per rank: reached nodes with that many children, and how
+// often the child of that rank was the accepted one).
 //
 // Recurrence.  With F(n, d) the best E of an n-node tree of depth <= d:
 //   F(1, d) = 1;  F(n > 1, 0) = -inf;
@@ -15,11 +18,12 @@
 //   nodes hung below a node as children of rank i, i+1, ... (each child of rank j with
 //   its own subtree of a nodes and depth <= d - 1 adds accept[j-1] * F(a, d - 1)):
 //     G_d(i, 0) = 0;   G_d(K + 1, m) = 0 (the m nodes become children of rank > K,
-//     leaves, never accepted);   G_d(i, m) = max over 1 <= a <= m of
-//     accept[i-1] * F(a, d - 1) + G_d(i + 1, m - a).
+//     leaves, never accepted);   G_d(i, m) = max over 1 <= a <= m with
+//     F(a, d - 1) > -inf of accept[i-1] * F(a, d - 1) + G_d(i + 1, m - a).
 // The ranks are filled in order, so a node's children occupy ranks 1, 2, ... with no
 // gap.  Cost O(D K n^2) for D = min(d_max, n_max - 1) levels and K = min(K, n_max - 1)
 // ranks: about 10^8 multiply-adds at n = 128, D = K = 127, a fraction of a second.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -187,6 +191,39 @@ tsv_status tsv_sequoia_plan(const double* accept, int K, int n_max, int d_max, c
     *n_best = bn;
     *d_best = bd;
     *speedup = best;
+    return TSV_OK;
+}
+
+tsv_status tsv_sequoia_accept_counts(const int32_t* parent, const int32_t* accepted_nodes, const int32_t* accept_len,
+                                     int B, int N, int K, int64_t* reached, int64_t* accepted) {
+    if (!parent || !accepted_nodes || !accept_len || !reached || !accepted)
+        return tsv::report_error(TSV_ERR_ARG, "null pointer");
+    if (B < 0 || N < 1 || N > kMaxTreeNodes || K < 1)
+        return tsv::report_error(TSV_ERR_ARG, "bad sizes B=%d N=%d K=%d", B, N, K);
+    std::vector<int> nkids(N), rank(N);
+    for (int b = 0; b < B; ++b) {
+        const int A = accept_len[b];
+        if (A < 0) continue;
+        const int32_t* par = parent + (size_t)b * N;
+        const int32_t* path = accepted_nodes + (size_t)b * N;
+        if (par[0] != -1) return tsv::report_error(TSV_ERR_ARG, "sequence %d: parent[0] != -1", b);
+        std::fill(nkids.begin(), nkids.end(), 0);
+        for (int i = 1; i < N; ++i) {
+            if (par[i] < 0 || par[i] >= i) return tsv::report_error(TSV_ERR_ARG, "sequence %d: bad parent[%d]", b, i);
+            rank[i] = ++nkids[par[i]];  // children in index order: the order the walk tries them
+        }
+        if (A >= N || path[0] != 0) return tsv::report_error(TSV_ERR_ARG, "sequence %d: bad accepted path", b);
+        for (int j = 0; j <= A; ++j) {
+            const int v = path[j];
+            for (int k = 0; k < nkids[v] && k < K; ++k) ++reached[k];
+            if (j < A) {
+                const int c = path[j + 1];
+                if (c <= 0 || c >= N || par[c] != v)
+                    return tsv::report_error(TSV_ERR_ARG, "sequence %d: accepted path leaves the tree", b);
+                if (rank[c] <= K) ++accepted[rank[c] - 1];
+            }
+        }
+    }
     return TSV_OK;
 }
 
