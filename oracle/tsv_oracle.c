@@ -20,7 +20,11 @@
  *    accepted run takes one more token from the next-token distribution.
  *  - "Sequoia: Scalable and Robust Speculative Decoding" summary, sections
  *    "Scalable Speculative Decoding" and "Robust Sampling": siblings are verified
- *    as sampling without replacement.
+ *    as sampling without replacement; its figure comparing the rejection rates of
+ *    the SEQUOIA, SpecInfer, SpecTr and top-k verification algorithms: the
+ *    SpecInfer variant, read here as siblings drafted independently (with
+ *    replacement) from q and verified with the residual update alone, q kept
+ *    (with_replacement = 1; the library does not offer this walk yet).
  *  - SGLang "SpeculativeDecoding" page, section "Speculative Decoding" (full /
  *    no / prefix match; rejected tokens' KV cache is evicted).
  *
@@ -35,7 +39,7 @@
  *  - accept iff u < p(x)/q(x) with u in [0,1); q(x) == 0 accepts iff p(x) > 0;
  *  - after a rejected sibling with token x: p <- normalize(max(0, p - q)) (if that
  *    sum is zero, p is kept), q(x) <- 0 and q <- normalize(q) (if that sum is zero,
- *    q is kept), then the next sibling is tried;
+ *    q is kept), then the next sibling is tried (with replacement: q is kept);
  *  - the bonus token is the smallest t with u_bonus < sum_{v<=t} p(v) (inverse CDF
  *    in token order); if there is none, the last t with p(t) > 0;
  *  - at T == 0 a child is accepted iff its token is the argmax of the logits row
@@ -243,7 +247,7 @@ int oracle_tree_reject_sample(const float *target_logits, const float *draft_pro
                               const float *u_accept, const float *u_bonus, float temperature,
                               int B, int N, int V, int32_t *accepted_nodes, int32_t *accept_len,
                               int32_t *bonus_token, int32_t *out_tokens, double *ratio,
-                              double *bonus_cdf, int32_t *seq_err)
+                              double *bonus_cdf, int32_t *seq_err, int with_replacement)
 {
     if (B < 0 || N < 1 || V < 1 || !(temperature >= 0.0f) || !isfinite(temperature))
         return -1;
@@ -361,16 +365,17 @@ int oracle_tree_reject_sample(const float *target_logits, const float *draft_pro
                     for (int v = 0; v < V; v++)
                         p[v] = fmax(0.0, p[v] - qv[v]) / zr;
 #endif
-                /* without replacement: q(x) <- 0, q <- normalize(q) */
-#if ORACLE_MUTANT != 1
-                qv[x] = 0.0; /* mutant 1 keeps q fixed (with-replacement test) */
-#endif
-                double zq = 0.0;
-                for (int v = 0; v < V; v++)
-                    zq += qv[v];
-                if (zq > 0.0)
+                /* without replacement: q(x) <- 0, q <- normalize(q); with replacement
+                 * the next sibling was drawn from the same q, which is kept */
+                if (!with_replacement) {
+                    qv[x] = 0.0;
+                    double zq = 0.0;
                     for (int v = 0; v < V; v++)
-                        qv[v] /= zq;
+                        zq += qv[v];
+                    if (zq > 0.0)
+                        for (int v = 0; v < V; v++)
+                            qv[v] /= zq;
+                }
             }
             if (err || next < 0)
                 break;

@@ -12,8 +12,11 @@
   * T = 0 reduces to greedy argmax matching, checked against an independent walk;
   * no match returns exactly one target token, and the page's prefix-match example
     ("and it's so hot" vs "and it's very warm") keeps the first two drafts.
-Planted mistakes (q kept fixed between siblings, residual left unnormalised,
-residual skipped) must fail the chi-square pin.
+Planted mistakes (residual left unnormalised, residual skipped) and the walk for
+independent drafts applied to siblings drafted without replacement must fail the
+chi-square pin.  The walk for siblings drafted independently from q (with
+replacement, q kept after a rejection -- the SpecInfer variant the Sequoia summary
+compares against) passes it on such drafts, where the without-replacement walk fails.
 """
 import json
 import os
@@ -81,10 +84,11 @@ def test_hand_worked_cases(oracle_mod, case):
 
 # ----------------------------------------------------------------------------- losslessness
 
-def _markov_trials(rng, n, parent, V, T, tgt_table, drf_table, x0):
+def _markov_trials(rng, n, parent, V, T, tgt_table, drf_table, x0, iid=False):
     """n independent verification trials of one tree topology.  The target and
     draft distributions after a node depend only on that node's token (a Markov
-    target), so the emitted chain must follow softmax(tgt_table[x] / T)."""
+    target), so the emitted chain must follow softmax(tgt_table[x] / T).  Siblings
+    are drafted without replacement (Gumbel top-k), or independently if iid."""
     N = len(parent)
     kids = [[] for _ in range(N)]
     for c in range(1, N):
@@ -95,6 +99,11 @@ def _markov_trials(rng, n, parent, V, T, tgt_table, drf_table, x0):
         if not kids[i]:
             continue
         q = drf_table[tok[:, i]].astype(np.float64)
+        if iid:
+            cdf = np.cumsum(q, axis=1)
+            u = rng.random((n, len(kids[i]))) * cdf[:, -1:]
+            tok[:, kids[i]] = np.minimum((u[:, :, None] >= cdf[:, None, :]).sum(axis=2), V - 1)
+            continue
         with np.errstate(divide="ignore"):
             key = np.log(q) + rng.gumbel(size=q.shape)
         top = np.argsort(-key, axis=1, kind="stable")[:, :len(kids[i])]
@@ -106,7 +115,8 @@ def _markov_trials(rng, n, parent, V, T, tgt_table, drf_table, x0):
     return _inp(logits, probs, tok, np.tile(parent, (n, 1)), ua, ub, T)
 
 
-def _chi2_pvalues(oracle_mod, parent, T, trials=1_000_000, chunk=200_000, seed=0, mutant=0, V=16):
+def _chi2_pvalues(oracle_mod, parent, T, trials=1_000_000, chunk=200_000, seed=0, mutant=0, V=16, iid=False,
+                  replacement=False):
     rng = np.random.default_rng(seed)
     tgt_table = rng.normal(0.0, 1.0, (V, V)).astype(np.float32)
     drf_logits = tgt_table + rng.normal(0.0, 0.8, (V, V)).astype(np.float32)
@@ -115,8 +125,8 @@ def _chi2_pvalues(oracle_mod, parent, T, trials=1_000_000, chunk=200_000, seed=0
     first = np.zeros(V, np.int64)
     pair = np.zeros((V, V), np.int64)
     for s in range(0, trials, chunk):
-        inp = _markov_trials(rng, min(chunk, trials - s), np.array(parent), V, T, tgt_table, drf_table, x0)
-        r = oracle_mod.tree_reject_sample(inp, mutant=mutant)
+        inp = _markov_trials(rng, min(chunk, trials - s), np.array(parent), V, T, tgt_table, drf_table, x0, iid=iid)
+        r = oracle_mod.tree_reject_sample(inp, mutant=mutant, replacement=replacement)
         assert not r["err"].any()
         ot = r["out_tokens"]
         if (ot[:, 0] < 0).any():  # no token emitted at all: not a distribution over the vocab
@@ -150,10 +160,27 @@ def test_output_follows_target_distribution(oracle_mod, parent, T):
     assert p2 > 1e-3, p2
 
 
-@pytest.mark.parametrize("mutant", [1, 2, 5])
+@pytest.mark.parametrize("mutant", [2, 5])
 def test_planted_sampler_mistakes_fail_chi_square(oracle_mod, mutant):
     p1, p2, _ = _chi2_pvalues(oracle_mod, SIBLINGS, 1.0, trials=400_000, mutant=mutant)
     assert min(p1, p2) < 1e-6, (p1, p2)
+
+
+def test_walk_must_match_how_siblings_were_drafted(oracle_mod):
+    # drafted without replacement: keeping q after a rejection is a mistake
+    p1, p2, _ = _chi2_pvalues(oracle_mod, SIBLINGS, 1.0, trials=400_000, replacement=True)
+    assert min(p1, p2) < 1e-6, (p1, p2)
+    # drafted independently from q: zeroing the rejected token in q is the mistake
+    p1, p2, _ = _chi2_pvalues(oracle_mod, SIBLINGS, 1.0, trials=400_000, iid=True)
+    assert min(p1, p2) < 1e-6, (p1, p2)
+
+
+@pytest.mark.parametrize("T", [1.0, 0.6])
+def test_with_replacement_walk_is_lossless_on_independent_drafts(oracle_mod, T):
+    p1, p2, first = _chi2_pvalues(oracle_mod, SIBLINGS, T, iid=True, replacement=True)
+    assert first.sum() == 1_000_000
+    assert p1 > 1e-3, p1
+    assert p2 > 1e-3, p2
 
 
 # ----------------------------------------------------------------------------- special cases
