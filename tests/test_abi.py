@@ -63,3 +63,42 @@ def test_error_bits_match_the_header():
                  "TSV_DERR_TIMEOUT"]:
         m = re.search(name + r"\s*=\s*(\d+)", text)
         assert m and int(m.group(1)) == getattr(tsv, name), name
+
+
+def test_every_refusal_happens_before_any_launch(lib):
+    """Each host-side check answers on a machine without a GPU: the fake (aligned,
+    never dereferenced) pointers below would fault if anything reached the device."""
+    P, A, M = None, 4096, 4104  # null, 16-byte aligned, misaligned
+    attn = lib.tsv_tree_verify_attn
+
+    def call(q=A, out=A, B=2, N=8, Hq=8, Hkv=2, D=64, bs=16, mb=4, nb=8, scale=0.125, dt=0, ws=P, wsb=0):
+        return attn(q, A, A, A, A, A, out, B, N, Hq, Hkv, D, bs, mb, nb, scale, dt, ws, wsb, A, P)
+
+    assert call(q=M) == tsv.TSV_ERR_ARG and b"aligned" in lib.tsv_last_error()
+    assert call(out=M) == tsv.TSV_ERR_ARG
+    for bad_scale in (0.0, -1.0, float("nan"), float("inf")):
+        assert call(scale=bad_scale) == tsv.TSV_ERR_ARG, bad_scale
+    assert call(N=128, Hq=64, Hkv=4) == tsv.TSV_ERR_UNSUPPORTED  # 2048 query rows per kv head
+    assert call(dt=5) == tsv.TSV_ERR_ARG
+    assert call(Hkv=0) == tsv.TSV_ERR_ARG
+    assert call(N=0) == tsv.TSV_ERR_ARG
+    assert call(bs=32 + 1) == tsv.TSV_ERR_UNSUPPORTED
+    assert call(B=0, q=P, out=P) == tsv.TSV_OK  # empty batch: nothing to do, nothing read
+
+    walk = lib.tsv_tree_reject_sample
+    arrs = [A] * 6
+    outs = [A] * 5
+    assert walk(*arrs, 1.0, 2, 8, 0, *outs, P) == tsv.TSV_ERR_ARG  # V = 0
+    assert walk(*arrs, 1.0, 2, 8, 16 * 512 * 32 + 1, *outs, P) == tsv.TSV_ERR_UNSUPPORTED
+    for bad_t in (float("nan"), float("inf"), -0.5):
+        assert walk(*arrs, bad_t, 2, 8, 100, *outs, P) == tsv.TSV_ERR_ARG, bad_t
+    assert walk(*arrs, 1.0, 2, 0, 100, *outs, P) == tsv.TSV_ERR_ARG  # no root
+    assert walk(*[P] * 6, 1.0, 0, 8, 100, *[P] * 5, P) == tsv.TSV_OK  # empty batch
+
+    comp = lib.tsv_kv_compact_accepted
+    assert comp(M, A, A, A, A, A, A, 2, 8, 2, 64, 16, 4, 8, 0, A, P) == tsv.TSV_ERR_ARG
+    assert comp(A, A, A, A, A, A, A, 2, 8, 2, 96, 16, 4, 8, 0, A, P) == tsv.TSV_ERR_UNSUPPORTED
+    assert comp(A, A, A, A, A, A, A, 2, 8, 2, 64, 16, 4, 8, 9, A, P) == tsv.TSV_ERR_ARG
+    assert comp(A, A, A, A, P, A, A, 2, 8, 2, 64, 16, 4, 8, 0, A, P) == tsv.TSV_ERR_ARG
+
+    assert lib.tsv_noalloc_scratch_bytes() == 64 << 20
