@@ -48,7 +48,8 @@ def _lib(mutant: int = 0):
         lib.oracle_tree_verify_attn.argtypes = [P, P, P, i32, P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                                 i32, f64, P, i64, P, P]
         lib.oracle_tree_verify_attn.restype = i32
-        lib.oracle_tree_reject_sample.argtypes = [P, P, P, P, P, P, f32, i32, i32, i32, P, P, P, P, P, P, P, i32]
+        lib.oracle_tree_reject_sample.argtypes = [P, P, P, P, P, P, f32, i32, i32, i32, P, P, P, P, P, P, P, i32, i32,
+                                                  f64]
         lib.oracle_tree_reject_sample.restype = i32
         lib.oracle_kv_compact_accepted.argtypes = [P, P, i32, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
                                                    i32, P]
@@ -91,12 +92,13 @@ def tree_verify_attn(inp: dict, rows: Optional[np.ndarray] = None, *, mutant: in
 
 
 def tree_reject_sample(inp: dict, *, temperature: Optional[float] = None, mutant: int = 0,
-                       replacement: bool = False) -> dict:
+                       replacement: bool = False, top_k: int = 0, top_p: float = 1.0) -> dict:
     """Literal sequential rejection-sampling walk in fp64.  Returns a dict with
     accepted_nodes [B,N], accept_len [B], bonus_token [B], out_tokens [B,N],
     ratio [B,N] (tried children; NaN otherwise), bonus_cdf [B,2], err [B].
     replacement=True: the walk for siblings drafted independently from q (q kept
-    after a rejection); the default is the without-replacement walk."""
+    after a rejection); the default is the without-replacement walk.  top_k / top_p
+    filter the target distribution p (top_k 0 and top_p 1: no filter)."""
     B, N, V = inp["B"], inp["N"], inp["V"]
     T = float(inp["T"] if temperature is None else temperature)
     logits = _c(inp["target_logits"], np.float32)
@@ -112,7 +114,7 @@ def tree_reject_sample(inp: dict, *, temperature: Optional[float] = None, mutant
     rc = _lib(mutant).oracle_tree_reject_sample(
         _ptr(logits), _ptr(probs), _ptr(tok), _ptr(par), _ptr(ua), _ptr(ub), T, B, N, V,
         _ptr(r["accepted_nodes"]), _ptr(r["accept_len"]), _ptr(r["bonus_token"]), _ptr(r["out_tokens"]),
-        _ptr(r["ratio"]), _ptr(r["bonus_cdf"]), _ptr(r["err"]), 1 if replacement else 0)
+        _ptr(r["ratio"]), _ptr(r["bonus_cdf"]), _ptr(r["err"]), 1 if replacement else 0, int(top_k), float(top_p))
     if rc != 0:
         raise ValueError("oracle_tree_reject_sample: bad arguments")
     return r

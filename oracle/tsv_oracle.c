@@ -42,6 +42,11 @@
  *    q is kept), then the next sibling is tried (with replacement: q is kept);
  *  - the bonus token is the smallest t with u_bonus < sum_{v<=t} p(v) (inverse CDF
  *    in token order); if there is none, the last t with p(t) > 0;
+ *  - top_k / top_p (the Sequoia summary's table of robustness to top-p; the library
+ *    does not offer them yet): p is first filtered to its top_k most probable tokens
+ *    and then to the smallest prefix of them, by decreasing p with ties to the lower
+ *    index, whose mass reaches top_p, and renormalised; q is the drafter's own
+ *    (already filtered) distribution as given;
  *  - at T == 0 a child is accepted iff its token is the argmax of the logits row
  *    (lowest index on ties), and the bonus is that argmax;
  *  - compaction copies the path's K/V rows to contiguous slots after the root and
@@ -231,6 +236,53 @@ static int row_is_finite(const float *row, int V)
     return 1;
 }
 
+/* Filtered target distribution (top-k / top-p): keep the top_k most probable tokens
+ * (top_k <= 0: all), then the smallest prefix of them, in order of decreasing p (ties:
+ * lower index first), whose mass reaches top_p of the row (top_p >= 1: all kept); zero
+ * the rest and renormalise.  tmp holds V (p, index) pairs. */
+typedef struct {
+    double p;
+    int v;
+} pv_t;
+
+static int pv_cmp(const void *a, const void *b)
+{
+    const pv_t *x = (const pv_t *)a, *y = (const pv_t *)b;
+    if (x->p != y->p)
+        return x->p > y->p ? -1 : 1;
+    return x->v - y->v;
+}
+
+static void filter_top(double *p, int V, int top_k, double top_p, pv_t *tmp)
+{
+    if (top_k <= 0 && top_p >= 1.0)
+        return;
+    for (int v = 0; v < V; v++) {
+        tmp[v].p = p[v];
+        tmp[v].v = v;
+    }
+    qsort(tmp, (size_t)V, sizeof(pv_t), pv_cmp);
+    int keep = (top_k > 0 && top_k < V) ? top_k : V;
+    if (top_p < 1.0) {
+        double cum = 0.0;
+        int n = 0;
+        while (n < keep) {
+            cum += tmp[n].p;
+            n++;
+            if (cum >= top_p)
+                break;
+        }
+        keep = n;
+    }
+    for (int v = 0; v < V; v++)
+        p[v] = 0.0;
+    double z = 0.0;
+    for (int n = 0; n < keep; n++)
+        z += tmp[n].p;
+    for (int n = 0; n < keep; n++)
+        p[tmp[n].v] = tmp[n].p / z;
+}
+
 /*
  * Rejection-sampling tree walk (one sequence after another).
  *
@@ -247,7 +299,8 @@ int oracle_tree_reject_sample(const float *target_logits, const float *draft_pro
                               const float *u_accept, const float *u_bonus, float temperature,
                               int B, int N, int V, int32_t *accepted_nodes, int32_t *accept_len,
                               int32_t *bonus_token, int32_t *out_tokens, double *ratio,
-                              double *bonus_cdf, int32_t *seq_err, int with_replacement)
+                              double *bonus_cdf, int32_t *seq_err, int with_replacement, int top_k,
+                              double top_p)
 {
     if (B < 0 || N < 1 || V < 1 || !(temperature >= 0.0f) || !isfinite(temperature))
         return -1;
@@ -256,6 +309,7 @@ int oracle_tree_reject_sample(const float *target_logits, const float *draft_pro
     double *p = malloc(sizeof(double) * (size_t)V);
     double *qv = malloc(sizeof(double) * (size_t)V);
     int32_t *path = malloc(sizeof(int32_t) * (size_t)N);
+    pv_t *pv = (top_k > 0 || top_p < 1.0) ? malloc(sizeof(pv_t) * (size_t)V) : NULL;
 
     for (int b = 0; b < B; b++) {
         const int32_t *par = parent + (int64_t)b * N;
@@ -303,6 +357,7 @@ int oracle_tree_reject_sample(const float *target_logits, const float *draft_pro
                 }
                 for (int v = 0; v < V; v++)
                     p[v] /= z;
+                filter_top(p, V, top_k, top_p, pv);
             }
             const float *qrow = draft_probs ? draft_probs + ((int64_t)b * N + i) * V : NULL;
             int next = -1;
@@ -433,6 +488,7 @@ int oracle_tree_reject_sample(const float *target_logits, const float *draft_pro
     }
     free(p);
     free(qv);
+    free(pv);
     free(path);
     return 0;
 }

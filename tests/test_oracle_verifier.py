@@ -291,3 +291,58 @@ def test_error_bits(oracle_mod):
     assert list(r["err"]) == [1, 8, 16, 16, 16, 0, 0]
     assert list(r["accept_len"][:5]) == [-1] * 5 and (r["accept_len"][5:] >= 0).all()
     assert (r["out_tokens"][:5] == -1).all() and (r["bonus_token"][:5] == -1).all()
+
+
+# ----------------------------------------------------------------------------- top-k / top-p
+
+def _filtered(p, top_k, top_p):
+    """The filtered target distribution, built directly: stable descending order."""
+    order = np.lexsort((np.arange(len(p)), -p))
+    keep = len(p) if top_k <= 0 else min(top_k, len(p))
+    if top_p < 1.0:
+        cum = np.cumsum(p[order[:keep]])
+        keep = int(np.searchsorted(cum, top_p, side="left")) + 1
+        keep = min(keep, len(cum))
+    out = np.zeros_like(p)
+    out[order[:keep]] = p[order[:keep]] / p[order[:keep]].sum()
+    return out
+
+
+def test_no_filter_is_the_plain_walk(oracle_mod):
+    w = W.CONFIGS[3].replace(B=32, Hq=4, Hkv=1, D=64, prefix=(0, 0), N=30, depth=6, V=500, T=1.0, seed=41)
+    inp = W.generate(w)
+    a = oracle_mod.tree_reject_sample(inp)
+    b = oracle_mod.tree_reject_sample(inp, top_k=0, top_p=1.0)
+    for key in ("accepted_nodes", "accept_len", "bonus_token", "out_tokens", "err"):
+        assert np.array_equal(a[key], b[key])
+
+
+def test_top1_reduces_to_greedy(oracle_mod):
+    # only the argmax keeps mass: a child is accepted iff it is the argmax (its q > 0
+    # makes the ratio >= 1 > u), and the bonus is the argmax -- the T = 0 walk
+    w = W.CONFIGS[3].replace(B=48, Hq=4, Hkv=1, D=64, prefix=(0, 0), N=25, depth=5, V=300, T=1.0, seed=43)
+    inp = W.generate(w)
+    a = oracle_mod.tree_reject_sample(inp, top_k=1)
+    g = oracle_mod.tree_reject_sample(inp, temperature=0.0)
+    for key in ("accepted_nodes", "accept_len", "bonus_token", "out_tokens"):
+        assert np.array_equal(a[key], g[key]), key
+
+
+@pytest.mark.parametrize("top_k,top_p", [(0, 0.8), (5, 1.0), (6, 0.6)])
+def test_filtered_output_follows_filtered_target(oracle_mod, top_k, top_p):
+    V, T, x0 = 16, 1.0, 3
+    rng = np.random.default_rng(17)
+    tgt_table = rng.normal(0.0, 1.0, (V, V)).astype(np.float32)
+    drf_logits = tgt_table + rng.normal(0.0, 0.8, (V, V)).astype(np.float32)
+    # the drafter samples from its own filtered distribution
+    drf_table = np.stack([_filtered(r, top_k, top_p) for r in _softmax64(drf_logits, T)]).astype(np.float32)
+    counts = np.zeros(V, np.int64)
+    for _ in range(3):
+        inp = _markov_trials(rng, 200_000, np.array(SIBLINGS), V, T, tgt_table, drf_table, x0)
+        r = oracle_mod.tree_reject_sample(inp, top_k=top_k, top_p=top_p)
+        assert not r["err"].any()
+        counts += np.bincount(r["out_tokens"][:, 0], minlength=V)
+    want = _filtered(_softmax64(tgt_table[x0], T), top_k, top_p)
+    assert np.all(counts[want == 0] == 0)
+    m = want > 0
+    assert stats.chisquare(counts[m], want[m] * counts.sum()).pvalue > 1e-3
