@@ -121,9 +121,14 @@ tsv_status tsv_tree_verify_attn(const void *q, const void *k_cache, const void *
  * process exits.  Nothing is allocated per call.
  *  - Shapes whose tsv_attn_workspace_size exceeds the array are rejected with
  *    TSV_ERR_UNSUPPORTED before anything is launched.
+ *  - The array used is the CURRENT device's: the current device must be the device
+ *    of `stream` and of every buffer (a stream of another device is refused with
+ *    TSV_ERR_ARG).
  *  - The first call on a device looks up the array's device address (once per
- *    device, with that device current); make that first call before any stream
- *    capture.
+ *    device, with that device current; again only if the device's context changes,
+ *    e.g. after cudaDeviceReset, which reloads the array with the module); make that
+ *    first call before any stream capture.  A failed lookup returns TSV_ERR_CUDA and
+ *    is retried by the next call.
  *  - All calls share the array: calls that overlap on the GPU race on it and must
  *    be ordered by the caller.  Each call rewrites every scratch byte it reads.
  * ------------------------------------------------------------------------- */
@@ -149,7 +154,8 @@ tsv_status tsv_tree_verify_attn_noalloc(const void *q, const void *k_cache, cons
  *                  q(x) <- 0, q <- normalize(q) (kept if that sum is 0);
  *   the first accepted child becomes i; when no child is accepted (or i is a
  *   leaf) the walk stops and the bonus token is the smallest t with
- *   u_bonus[b] < sum_{v<=t} p(v) over the current p (last t with p(t) > 0 if none).
+ *   u_bonus[b] < sum_{v<=t} p(v) over the current p; if there is none (u_bonus >= 1
+ *   or NaN, outside the stated [0, 1)), the last t with p(t) > 0.
  * T == 0: a child is accepted iff its token is argmax target_logits[b,i,:]
  * (lowest index on ties) and the bonus is that argmax; draft_probs and the
  * uniforms are not read (draft_probs may be NULL).

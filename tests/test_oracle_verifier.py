@@ -346,3 +346,28 @@ def test_filtered_output_follows_filtered_target(oracle_mod, top_k, top_p):
     assert np.all(counts[want == 0] == 0)
     m = want > 0
     assert stats.chisquare(counts[m], want[m] * counts.sum()).pvalue > 1e-3
+
+
+# ----------------------------------------------------------------------------- top of the unit interval
+
+@pytest.mark.parametrize("logits,u,want", [
+    ([0.0, 0.0, -1000.0, -1000.0], 1.0, 1),                  # p = [1/2, 1/2, 0, 0] exactly: u = 1 passes every boundary
+    ([0.0, 0.0, 0.0, -1000.0], 1.0, 2),                      # p = [1/3, 1/3, 1/3, 0]: the last token with mass
+    ([0.0, 0.0, -1000.0, -1000.0], float("nan"), 1),         # no boundary lies above NaN either
+    ([0.0, 0.0, -1000.0, -1000.0], np.nextafter(np.float32(1), np.float32(0)), 1),  # u < 1: the ordinary draw
+    ([0.0, 0.0, -1000.0, -1000.0], 0.5, 1),                  # u on the boundary sum_{v<=0} p = 1/2: strict '<'
+    ([0.0, 0.0, -1000.0, -1000.0], 0.49999997, 0),
+])
+def test_bonus_draw_at_the_top_of_the_unit_interval(oracle_mod, logits, u, want):
+    """Inverse CDF (statistical-learning-notes ch.07, "Draft Token Validation": a fully
+    accepted run draws one more token from the next-token distribution): the smallest
+    t with u < sum_{v<=t} p(v).  A u at or past the top of [0, 1) -- which a caller may
+    pass, and fp rounding of the sums could in principle reach -- passes every
+    boundary; the draw is then the inverse CDF's limit, the last token with p > 0
+    (never a token of zero probability).  exp(-1000) is 0 in fp64, so the p rows here
+    are exact."""
+    inp = _inp(np.array([[logits]]), np.full((1, 1, 4), 0.25), [[0]], [[-1]], [[0.0]], [u], 1.0)
+    r = oracle_mod.tree_reject_sample(inp)
+    assert r["err"][0] == 0 and r["accept_len"][0] == 0
+    assert r["bonus_token"][0] == want
+    assert list(r["out_tokens"][0]) == [want]

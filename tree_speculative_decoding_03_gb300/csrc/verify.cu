@@ -792,6 +792,48 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
             const float p = lv_is_p ? lv[k][e] * pscale : ex2(fmaf(lv[k][e], c2, -MC)) * invZf;
             pk[k][e] = (v < v1) ? p : 0.0f;
         }
+    if (!(a.u_bonus[b] < 1.0f)) {
+        // u at or past the top of [0, 1) (or NaN): no CDF boundary lies above it, so the
+        // draw is the inverse CDF's limit there, the last token with p > 0 (the same
+        // rule as the oracle's)
+        int last = -1;
+#pragma unroll
+        for (int k = 0; k < VEC; ++k)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int v = v0 + (k * (int)blockDim.x + tid) * 4 + e;
+                if (v < v1 && pk[k][e] > 0.0f) last = max(last, v);
+            }
+        float lv_ = last >= 0 ? (float)last : -INFINITY;  // indices < 2^24 are exact in fp32
+        warp_argmax(lv_, last);
+        if (lane == 0) {
+            s_wf[warp] = lv_;
+            s_wi[warp] = last;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            float v = lane < nwarps ? s_wf[lane] : -INFINITY;
+            int i = lane < nwarps ? s_wi[lane] : -1;
+            warp_argmax(v, i);
+            if (lane == 0) {
+                RedSlot m{};
+                m.a = v;
+                m.i = i;
+                s_cta = m;
+            }
+        }
+        __syncthreads();
+        cluster_allreduce(cluster, s_red, parity, s_cta, kRedArgmax, c2, &s_all);
+        parity ^= 1;
+        if (rank == 0 && tid == 0) {
+            const int tok = s_all.a > -INFINITY ? s_all.i : -1;
+            a.bonus_token[b] = tok;
+            a.out_tokens[rowoff + plen - 1] = tok;
+        }
+        cluster.sync();
+        if (a.k_cache && rank == 0) fused_compact(a, b, plen - 1, s_path, &s_flag, s_path, s_blkerr);
+        return;
+    }
 #pragma unroll
     for (int k = 0; k < VEC; ++k) {
         const float ts = warp_sum(pk[k][0] + pk[k][1] + pk[k][2] + pk[k][3]);
