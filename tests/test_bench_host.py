@@ -36,3 +36,30 @@ def test_replica_rate_uses_slowest_rank():
     port = 29500 + os.getpid() % 1000
     mp.spawn(_worker, args=(2, port, out), nprocs=2, join=True)
     assert out[0] == out[1] == 2 * 100.0 / 2.0
+
+
+def test_attention_flops():
+    inp = W.generate(W.CONFIGS[1].replace(B=2, V=64))
+    assert bench.attn_flops(inp) == 2 * 4 * 6 * 32 * 128 * (2048 + 6)
+
+
+def test_parity_summary_counts_identical_exempt_and_mismatched():
+    import oracle
+    inp = W.generate(W.CONFIGS[3].replace(B=6, Hq=4, Hkv=1, D=64, prefix=(0, 0), N=20, depth=5, V=300, seed=5))
+    o = oracle.tree_reject_sample(inp)
+    g = {k: v.copy() for k, v in o.items()}
+    # seq 1: a different bonus with u_bonus moved onto the oracle's CDF boundary -> exempt near tie
+    lo, hi = o["bonus_cdf"][1]
+    inp["u_bonus"] = inp["u_bonus"].copy()
+    inp["u_bonus"][1] = np.float32(hi)
+    g["bonus_token"][1] += 1
+    # seq 2: a different bonus far from any boundary -> mismatched
+    inp["u_bonus"][2] = np.float32(0.5 * (o["bonus_cdf"][2][0] + o["bonus_cdf"][2][1]))
+    g["bonus_token"][2] += 1
+    rows = np.array([0, 3])
+    want = np.zeros((2, 64))
+    got = np.zeros((inp["B"] * inp["N"] * inp["Hq"], 64))
+    got[3, 5] = 0.01
+    p = bench.parity_summary(inp, g, o, rows, want, got)
+    assert (p["identical"], p["exempt_near_ties"], p["mismatched"]) == (4, 1, 1)
+    assert p["attn_max_abs_err"] == 0.01 and not p["ok"]

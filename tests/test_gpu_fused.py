@@ -61,3 +61,45 @@ def test_trees_with_flagged_sequences(dtype, D):
     r = _same(inp)
     assert r["al"][2] == -1 and r["cerr"][2] == 0 and r["nl"][2] == inp["seq_lens"][2]
     assert r["cerr"][6] == tsv.TSV_DERR_BLOCK and r["nl"][6] == inp["seq_lens"][6]
+
+
+def _against_oracle(inp, T=None):
+    """The fused call against the oracle: its walk decisions against the oracle's walk
+    (bit-exact up to counted near ties), then the caches, new lengths and rewrite errors
+    against the oracle's array copy applied to the path the walk took."""
+    import oracle
+    from gpu_util import compare_decisions
+
+    T = inp["T"] if T is None else T
+    r = _run(inp, True, T)
+    o = oracle.tree_reject_sample(inp, temperature=T)
+    g = dict(accepted_nodes=r["an"], accept_len=r["al"], bonus_token=r["bt"], out_tokens=r["ot"], err=r["err"])
+    exempt, fails = compare_decisions(inp, g, o, T)
+    B = inp["B"]
+    msg = f"{exempt} of {B} sequences exempt as near ties; {len(fails)} mismatches: {fails[:5]}"
+    assert not fails, msg
+    assert exempt <= 0.05 * B + 1, msg
+    print(msg)
+    ok_, ov, ol, oe = oracle.kv_compact_accepted(inp, r["an"], r["al"])
+    assert np.array_equal(r["cerr"], oe), (r["cerr"], oe)
+    assert np.array_equal(r["nl"], ol), (r["nl"], ol)
+    assert np.array_equal(r["k"].reshape(-1), ok_.reshape(-1).view(np.uint8)), "K cache differs from the oracle's"
+    assert np.array_equal(r["v"].reshape(-1), ov.reshape(-1).view(np.uint8)), "V cache differs from the oracle's"
+    return r, o, exempt
+
+
+@pytest.mark.parametrize("T", [0.0, 0.6, 1.0])
+@pytest.mark.parametrize("dtype,D", [("bf16", 128), ("f32", 64)])
+def test_random_trees_against_the_oracle(T, dtype, D):
+    w = W.CONFIGS[3].replace(B=20, Hq=8, Hkv=2, D=D, dtype=dtype, prefix=(0, 700), N=40, depth=7, V=3001, T=T,
+                             seed=60 + int(10 * T) + D)
+    _against_oracle(W.generate(w, temperature=T), T)
+
+
+@pytest.mark.parametrize("cfg,T", [(1, 0.0), (1, 1.0), (2, None), (3, None), (4, None)])
+def test_full_size_against_the_oracle(cfg, T):
+    """The call the benchmark times, on the full workloads it times."""
+    inp = W.generate(W.CONFIGS[cfg], temperature=T)
+    r, o, _ = _against_oracle(inp, T)
+    if cfg == 4:  # the p == q sequences accept every draft down to a leaf
+        assert all(o["accept_len"][b] >= 1 for b in inp["pq_seqs"])

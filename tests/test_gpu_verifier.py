@@ -153,3 +153,28 @@ def test_chi_square_losslessness_on_gpu(T):
 def test_full_size(cfg, T):
     inp = W.generate(W.CONFIGS[cfg], temperature=T)
     _check(inp, T)
+
+
+def test_bonus_draw_at_the_top_of_the_unit_interval_on_gpu():
+    """u_bonus at or past 1 (and NaN) gives the last token with p > 0, as the oracle
+    does; compared exactly (no near-tie exemption applies to this rule)."""
+    w = W.CONFIGS[1].replace(B=16, Hq=4, Hkv=1, D=64, prefix=(0, 0), N=4, V=5000, seed=71)
+    inp = W.generate(w)
+    inp["target_logits"] = inp["target_logits"].copy()
+    inp["target_logits"][:, :, 4900:] = -1000.0        # no mass on the last 100 tokens
+    inp["target_logits"][1::2, :, 4000:4900] = -1000.0  # odd sequences: none past token 3999 either
+    inp["u_bonus"] = inp["u_bonus"].copy()
+    inp["u_bonus"][0::3] = 1.0
+    inp["u_bonus"][1::3] = np.nan
+    for T in (1.0, 0.6):
+        g = run_verify(inp, temperature=T)
+        o = oracle.tree_reject_sample(inp, temperature=T)
+        top = ~(inp["u_bonus"] < 1.0)
+        assert top.sum() >= 10
+        for key in ("accepted_nodes", "accept_len", "bonus_token", "out_tokens", "err"):
+            assert np.array_equal(g[key][top], o[key][top]), key
+        assert (o["bonus_token"][top] < np.where(np.arange(16)[top] % 2 == 1, 4000, 4900)).all()
+        exempt, fails = compare_decisions(
+            {k: (v[~top] if isinstance(v, np.ndarray) and v.shape[:1] == (16,) else v) for k, v in inp.items()},
+            {k: v[~top] for k, v in g.items()}, {k: v[~top] for k, v in o.items()}, T)
+        assert not fails, fails

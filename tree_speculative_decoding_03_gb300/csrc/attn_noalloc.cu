@@ -14,10 +14,19 @@
 // or from different host threads) race on it, so callers must order them.  Every
 // byte a call reads there (partials, per-unit records) is written earlier in the same
 // call, so nothing in it needs clearing between calls.
+//
+// Host code cannot pass the array's name to a kernel (on the host it names a
+// stand-in, not device memory): the array's device address is looked up with
+// cudaGetSymbolAddress, with the device current, the first time a device's context
+// calls this entry point.  The address is kept per device together with the context
+// it belongs to, and looked up again if that context changes (after cudaDeviceReset
+// the module, and with it the array, is loaded anew); a failed lookup is not kept.
 #include <cstdarg>
 #include <cstdio>
 #include <mutex>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "../../include/tsv.h"
@@ -33,9 +42,28 @@ constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_attn_scratch[kScratchBytes];
 
-void* g_scratch_addr[kMaxDevices];
-cudaError_t g_setup_status[kMaxDevices];
-std::once_flag g_setup_once[kMaxDevices];
+struct DeviceScratch {
+    std::mutex mu;
+    void* addr = nullptr;     // device address of g_attn_scratch in `ctx`
+    CUcontext ctx = nullptr;  // the context the address belongs to
+};
+DeviceScratch g_dev[kMaxDevices];
+
+// The calling thread's current driver context (the runtime's primary context after
+// any runtime call), through the driver entry point the runtime hands out.
+CUcontext current_context() {
+    static PFN_cuCtxGetCurrent_v4000 fn = []() -> PFN_cuCtxGetCurrent_v4000 {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+    }();
+    CUcontext c = nullptr;
+    if (fn == nullptr || fn(&c) != CUDA_SUCCESS) return nullptr;
+    return c;
+}
 
 }  // namespace
 
@@ -57,14 +85,34 @@ extern "C" tsv_status tsv_tree_verify_attn_noalloc(const void* q, const void* k_
                                  "tree_verify_attn_noalloc: this shape needs %zu bytes of scratch, more than the "
                                  "%zu-byte built-in array; use tsv_tree_verify_attn with a caller workspace",
                                  need, kScratchBytes);
-    // once per device, with that device current: the device address of the array
-    std::call_once(g_setup_once[dev], [dev]() {
-        g_setup_status[dev] = cudaGetSymbolAddress(&g_scratch_addr[dev], g_attn_scratch);
-    });
-    if (g_setup_status[dev] != cudaSuccess)
-        return tsv::report_error(TSV_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s",
-                                 cudaGetErrorString(g_setup_status[dev]));
+    if (reinterpret_cast<uintptr_t>(stream) > 2) {  // not a special handle (NULL, legacy, per-thread)
+        // the array used is the current device's: the stream must belong to that device
+        int sdev = -1;
+        e = cudaStreamGetDevice(static_cast<cudaStream_t>(stream), &sdev);
+        if (e != cudaSuccess) return tsv::report_error(TSV_ERR_CUDA, "cudaStreamGetDevice: %s", cudaGetErrorString(e));
+        if (sdev != dev)
+            return tsv::report_error(TSV_ERR_ARG,
+                                     "tree_verify_attn_noalloc: the stream belongs to device %d but device %d is "
+                                     "current; make the stream's device current",
+                                     sdev, dev);
+    }
+    void* scratch = nullptr;
+    {
+        DeviceScratch& s = g_dev[dev];
+        std::lock_guard<std::mutex> lock(s.mu);
+        const CUcontext ctx = current_context();
+        if (s.addr == nullptr || s.ctx != ctx) {
+            // set-up for this device (and context), with the device current
+            void* p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_attn_scratch);
+            if (e != cudaSuccess)
+                return tsv::report_error(TSV_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+            s.addr = p;
+            s.ctx = ctx;
+        }
+        scratch = s.addr;
+    }
     return tsv_tree_verify_attn(q, k_cache, v_cache, block_table, seq_lens, parent, out, B, N, Hq, Hkv, D,
-                                block_size, max_blocks, num_blocks, scale, dtype, g_scratch_addr[dev], kScratchBytes,
-                                seq_err, stream);
+                                block_size, max_blocks, num_blocks, scale, dtype, scratch, kScratchBytes, seq_err,
+                                stream);
 }
