@@ -177,6 +177,43 @@ tsv_status tsv_tree_reject_sample(const float *target_logits, const float *draft
                                   void *stream);
 
 /* ---------------------------------------------------------------------------
+ * Variants of the walk (a host struct, read during the call; NULL = the defaults
+ * {0, TSV_F32, 0, 1.0f}, i.e. tsv_tree_reject_sample).
+ *
+ * with_replacement: how the caller's drafter drew the siblings of a node.
+ *   0 -- without replacement (Sequoia summary, "Robust Sampling"): the walk above.
+ *   1 -- independently from q (the SpecInfer verification that the Sequoia summary's
+ *        figure of rejection rates compares against, "More on figures"): after a
+ *        rejected sibling only p takes the residual update, p <- normalize(max(0,
+ *        p - q)); q is kept (no q(x) <- 0), so siblings may repeat a token.
+ *   The walk must match the drafting: each is lossless only for its own drafts.
+ * logits_dtype: element type of target_logits, TSV_F32 or TSV_BF16 (the target
+ *   model's own output dtype; a bf16 row is half the bytes of an fp32 one).  A bf16
+ *   logit is decoded exactly to fp32; everything after the load is the fp32 walk.
+ * top_k, top_p: filtered target (the Sequoia summary's table of robustness to
+ *   top-p sampling, "More on tables"): at every visited node p is first restricted
+ *   to its top_k most probable tokens (top_k = 0: all), then to the smallest prefix
+ *   of them, by decreasing p with ties to the lower index, whose mass reaches top_p
+ *   (top_p = 1: all), and renormalised; q is the drafter's own (filtered)
+ *   distribution as given.  Not built yet: nonzero top_k or top_p < 1 return
+ *   TSV_ERR_UNSUPPORTED.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    int with_replacement;
+    tsv_dtype logits_dtype;
+    int top_k;
+    float top_p;
+} tsv_walk_options;
+
+/* tsv_tree_reject_sample with options; target_logits has opts->logits_dtype. */
+tsv_status tsv_tree_reject_sample_ex(const void *target_logits, const float *draft_probs,
+                                     const int32_t *draft_tokens, const int32_t *parent,
+                                     const float *u_accept, const float *u_bonus, float temperature,
+                                     const tsv_walk_options *opts, int B, int N, int V,
+                                     int32_t *accepted_nodes, int32_t *accept_len, int32_t *bonus_token,
+                                     int32_t *out_tokens, int32_t *seq_err, void *stream);
+
+/* ---------------------------------------------------------------------------
  * KV-cache rewrite for the accepted path (sglang report: the KV cache must be
  * updated selectively for accepted indices and trees require a rewrite; SGLang
  * "SpeculativeDecoding", prefix match: rejected tokens' KV cache is evicted).
@@ -213,6 +250,18 @@ tsv_status tsv_tree_reject_sample_compact(const float *target_logits, const floa
                                           const int32_t *seq_lens, int32_t *new_seq_lens, int Hkv,
                                           int D, int block_size, int max_blocks, int num_blocks,
                                           tsv_dtype dtype, int32_t *compact_err, void *stream);
+
+/* tsv_tree_reject_sample_compact with the walk options above. */
+tsv_status tsv_tree_reject_sample_compact_ex(const void *target_logits, const float *draft_probs,
+                                             const int32_t *draft_tokens, const int32_t *parent,
+                                             const float *u_accept, const float *u_bonus, float temperature,
+                                             const tsv_walk_options *opts, int B, int N, int V,
+                                             int32_t *accepted_nodes, int32_t *accept_len,
+                                             int32_t *bonus_token, int32_t *out_tokens, int32_t *seq_err,
+                                             void *k_cache, void *v_cache, const int32_t *block_table,
+                                             const int32_t *seq_lens, int32_t *new_seq_lens, int Hkv, int D,
+                                             int block_size, int max_blocks, int num_blocks, tsv_dtype dtype,
+                                             int32_t *compact_err, void *stream);
 
 /* ---------------------------------------------------------------------------
  * Tree construction (host side).  Sequoia summary, sections "Scalable Speculative

@@ -49,7 +49,7 @@ def _lib(mutant: int = 0):
                                                 i32, f64, P, i64, P, P]
         lib.oracle_tree_verify_attn.restype = i32
         lib.oracle_tree_reject_sample.argtypes = [P, P, P, P, P, P, f32, i32, i32, i32, P, P, P, P, P, P, P, i32, i32,
-                                                  f64]
+                                                  f64, i32]
         lib.oracle_tree_reject_sample.restype = i32
         lib.oracle_kv_compact_accepted.argtypes = [P, P, i32, P, P, P, P, P, i32, i32, i32, i32, i32, i32,
                                                    i32, P]
@@ -98,10 +98,12 @@ def tree_reject_sample(inp: dict, *, temperature: Optional[float] = None, mutant
     ratio [B,N] (tried children; NaN otherwise), bonus_cdf [B,2], err [B].
     replacement=True: the walk for siblings drafted independently from q (q kept
     after a rejection); the default is the without-replacement walk.  top_k / top_p
-    filter the target distribution p (top_k 0 and top_p 1: no filter)."""
+    filter the target distribution p (top_k 0 and top_p 1: no filter).  target_logits
+    may be float32 or bfloat16 bit patterns (uint16), which are decoded exactly."""
     B, N, V = inp["B"], inp["N"], inp["V"]
     T = float(inp["T"] if temperature is None else temperature)
-    logits = _c(inp["target_logits"], np.float32)
+    bf16_logits = inp["target_logits"].dtype == np.uint16  # bfloat16 bit patterns
+    logits = _c(inp["target_logits"], np.uint16 if bf16_logits else np.float32)
     probs = None if inp.get("draft_probs") is None else _c(inp["draft_probs"], np.float32)
     tok = _c(inp["draft_tokens"], np.int32)
     par = _c(inp["parent"], np.int32)
@@ -114,7 +116,8 @@ def tree_reject_sample(inp: dict, *, temperature: Optional[float] = None, mutant
     rc = _lib(mutant).oracle_tree_reject_sample(
         _ptr(logits), _ptr(probs), _ptr(tok), _ptr(par), _ptr(ua), _ptr(ub), T, B, N, V,
         _ptr(r["accepted_nodes"]), _ptr(r["accept_len"]), _ptr(r["bonus_token"]), _ptr(r["out_tokens"]),
-        _ptr(r["ratio"]), _ptr(r["bonus_cdf"]), _ptr(r["err"]), 1 if replacement else 0, int(top_k), float(top_p))
+        _ptr(r["ratio"]), _ptr(r["bonus_cdf"]), _ptr(r["err"]), 1 if replacement else 0, int(top_k), float(top_p),
+        DTYPE_CODE["bf16" if bf16_logits else "f32"])
     if rc != 0:
         raise ValueError("oracle_tree_reject_sample: bad arguments")
     return r

@@ -24,7 +24,7 @@
  *    the SEQUOIA, SpecInfer, SpecTr and top-k verification algorithms: the
  *    SpecInfer variant, read here as siblings drafted independently (with
  *    replacement) from q and verified with the residual update alone, q kept
- *    (with_replacement = 1; the library does not offer this walk yet).
+ *    (with_replacement = 1).
  *  - SGLang "SpeculativeDecoding" page, section "Speculative Decoding" (full /
  *    no / prefix match; rejected tokens' KV cache is evicted).
  *
@@ -284,7 +284,8 @@ static void filter_top(double *p, int V, int top_k, double top_p, pv_t *tmp)
 }
 
 /*
- * Rejection-sampling tree walk (one sequence after another).
+ * Rejection-sampling tree walk (one sequence after another).  target_logits is
+ * float32 (logits_dtype = DT_F32) or bfloat16 bits (DT_BF16).
  *
  * Outputs per sequence b: accepted_nodes[b, 0..] = root-first path (-1 padded),
  * accept_len[b] = drafts accepted (path length - 1), bonus_token[b], and
@@ -294,19 +295,20 @@ static void filter_top(double *p, int V, int top_k, double top_p, pv_t *tmp)
  * that was tried (NaN otherwise; +inf when q(x) == 0 < p(x)); bonus_cdf[b] =
  * (sum_{v<t} p(v), sum_{v<=t} p(v)) around the bonus token t (T > 0 only).
  */
-int oracle_tree_reject_sample(const float *target_logits, const float *draft_probs,
+int oracle_tree_reject_sample(const void *target_logits, const float *draft_probs,
                               const int32_t *draft_tokens, const int32_t *parent,
                               const float *u_accept, const float *u_bonus, float temperature,
                               int B, int N, int V, int32_t *accepted_nodes, int32_t *accept_len,
                               int32_t *bonus_token, int32_t *out_tokens, double *ratio,
                               double *bonus_cdf, int32_t *seq_err, int with_replacement, int top_k,
-                              double top_p)
+                              double top_p, int logits_dtype)
 {
     if (B < 0 || N < 1 || V < 1 || !(temperature >= 0.0f) || !isfinite(temperature))
         return -1;
     const int greedy = (temperature == 0.0f);
     const double T = (double)temperature;
     double *p = malloc(sizeof(double) * (size_t)V);
+    float *rowbuf = malloc(sizeof(float) * (size_t)V); /* the visited logits row, decoded */
     double *qv = malloc(sizeof(double) * (size_t)V);
     int32_t *path = malloc(sizeof(int32_t) * (size_t)N);
     pv_t *pv = (top_k > 0 || top_p < 1.0) ? malloc(sizeof(pv_t) * (size_t)V) : NULL;
@@ -340,7 +342,16 @@ int oracle_tree_reject_sample(const float *target_logits, const float *draft_pro
         path[plen++] = 0;
         const float *row = NULL;
         for (;;) {
-            row = target_logits + ((int64_t)b * N + i) * V;
+            /* bf16 logits decode exactly to float (the 16 bits are the top of a float) */
+            for (int v = 0; v < V; v++)
+#if ORACLE_MUTANT == 7 /* mistake: bf16 bits converted as an integer value, not reinterpreted */
+                rowbuf[v] = logits_dtype == DT_F32
+                                ? ((const float *)target_logits)[((int64_t)b * N + i) * V + v]
+                                : (float)((const uint16_t *)target_logits)[((int64_t)b * N + i) * V + v];
+#else
+                rowbuf[v] = (float)load_elem(target_logits, logits_dtype, ((int64_t)b * N + i) * V + v);
+#endif
+            row = rowbuf;
             if (!row_is_finite(row, V)) {
                 err = ERR_NONFINITE;
                 break;
@@ -487,6 +498,7 @@ int oracle_tree_reject_sample(const float *target_logits, const float *draft_pro
         bonus_token[b] = bonus;
     }
     free(p);
+    free(rowbuf);
     free(qv);
     free(pv);
     free(path);

@@ -30,7 +30,9 @@ def device_inputs(inp, attn=True, verify=True):
         d.update(q=kv(inp["q"]), k_cache=kv(inp["k_cache"]), v_cache=kv(inp["v_cache"]),
                  block_table=dev(inp["block_table"]), seq_lens=dev(inp["seq_lens"]))
     if verify:
-        d.update(target_logits=dev(inp["target_logits"]), draft_probs=dev(inp["draft_probs"]),
+        tl = inp["target_logits"]
+        d.update(target_logits=dev(tl.view(np.int16), torch.bfloat16) if tl.dtype == np.uint16 else dev(tl),
+                 draft_probs=dev(inp["draft_probs"]),
                  draft_tokens=dev(inp["draft_tokens"]), u_accept=dev(inp["u_accept"]), u_bonus=dev(inp["u_bonus"]))
     return d
 
@@ -49,8 +51,12 @@ def run_attn(inp, d=None):
     return out.float().cpu().numpy().reshape(B * N * Hq, D).astype(np.float64), err.cpu().numpy()
 
 
-def run_verify(inp, d=None, temperature=None):
+def run_verify(inp, d=None, temperature=None, **opts):
+    """The walk on the device (opts: with_replacement, top_k, top_p).  Target logits
+    given as uint16 are bfloat16 bit patterns."""
     d = d or device_inputs(inp, attn=False)
+    if d["target_logits"].dtype == torch.int16:
+        d["target_logits"] = d["target_logits"].view(torch.bfloat16)
     B, N, V = d["target_logits"].shape
     T = inp["T"] if temperature is None else temperature
     an = torch.full((B, N), -9, dtype=torch.int32, device="cuda")
@@ -59,7 +65,7 @@ def run_verify(inp, d=None, temperature=None):
     ot = torch.full((B, N), -9, dtype=torch.int32, device="cuda")
     err = torch.full((B,), -9, dtype=torch.int32, device="cuda")
     tsv.tree_reject_sample(d["target_logits"], d["draft_probs"], d["draft_tokens"], d["parent"], d["u_accept"],
-                           d["u_bonus"], T, an, al, bt, ot, err)
+                           d["u_bonus"], T, an, al, bt, ot, err, **opts)
     torch.cuda.synchronize()
     return dict(accepted_nodes=an.cpu().numpy(), accept_len=al.cpu().numpy(), bonus_token=bt.cpu().numpy(),
                 out_tokens=ot.cpu().numpy(), err=err.cpu().numpy())

@@ -49,6 +49,14 @@ def test_host_argument_checks_need_no_gpu(lib):
     assert fused(*[16] * 6, 0.0, 4, 8, 100, *fake, *fake, 2, 64, 12, 4, 8, 0, 16, P) == tsv.TSV_ERR_UNSUPPORTED
     assert fused(*[16] * 6, 0.0, 4, 8, 100, *fake, *[P] * 5, 2, 64, 16, 4, 8, 0, P, P) == tsv.TSV_ERR_ARG
     assert fused(*walk, 1.0, 0, 8, 100, *[P] * 5, *[P] * 5, 2, 64, 16, 4, 8, 0, P, P) == tsv.TSV_OK
+    # walk options: checked before anything else is looked at
+    from tree_speculative_decoding_03_gb300 import WalkOptions
+    ex = lib.tsv_tree_reject_sample_ex
+    for opts, want in ((WalkOptions(2, 1, 0, 1.0), tsv.TSV_ERR_ARG), (WalkOptions(0, 7, 0, 1.0), tsv.TSV_ERR_ARG),
+                       (WalkOptions(0, 1, -1, 1.0), tsv.TSV_ERR_ARG), (WalkOptions(0, 1, 0, 0.0), tsv.TSV_ERR_ARG),
+                       (WalkOptions(0, 1, 0, 1.5), tsv.TSV_ERR_ARG)):
+        assert ex(*[16] * 6, 1.0, ctypes.byref(opts), 4, 8, 100, *[16] * 5, P) == want
+    assert ex(*walk, 1.0, None, 0, 8, 100, *[P] * 5, P) == tsv.TSV_OK  # NULL options, empty batch
     # single-chunk plans need no workspace
     assert lib.tsv_attn_workspace_size(1, 15, 8, 2, 64, 16, 16, tsv.TSV_F32) == 0
     assert lib.tsv_attn_workspace_size(1, 15, 8, 2, 64, 16, 17, tsv.TSV_F32) > 0  # prefix may need 2 chunks

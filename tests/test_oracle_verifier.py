@@ -371,3 +371,23 @@ def test_bonus_draw_at_the_top_of_the_unit_interval(oracle_mod, logits, u, want)
     assert r["err"][0] == 0 and r["accept_len"][0] == 0
     assert r["bonus_token"][0] == want
     assert list(r["out_tokens"][0]) == [want]
+
+
+# ----------------------------------------------------------------------------- bf16 target logits
+
+@pytest.mark.parametrize("T", [0.0, 0.6, 1.0])
+def test_bf16_logits_walk_is_the_walk_on_their_exact_decode(oracle_mod, T):
+    """bf16 target logits (vLLM PR #2188, "Usage": the target model's output dtype) carry
+    the top 16 bits of a float32; the walk on them must be the walk on those floats,
+    decoded here independently of the oracle (bits << 16, reinterpreted).  A decode that
+    converts the 16-bit pattern as an integer (planted mistake 7) fails."""
+    w = W.CONFIGS[3].replace(B=40, Hq=4, Hkv=1, D=64, prefix=(0, 0), N=24, depth=6, V=700, T=T, seed=77)
+    inp = W.generate(w, temperature=T)
+    bits = W.f32_to_bf16_bits(inp["target_logits"])
+    dec = (bits.astype(np.uint32) << 16).view(np.float32)
+    a = oracle_mod.tree_reject_sample(dict(inp, target_logits=bits))
+    b = oracle_mod.tree_reject_sample(dict(inp, target_logits=dec))
+    for key in ("accepted_nodes", "accept_len", "bonus_token", "out_tokens", "err"):
+        assert np.array_equal(a[key], b[key]), key
+    m = oracle_mod.tree_reject_sample(dict(inp, target_logits=bits), mutant=7)
+    assert not all(np.array_equal(m[k], b[k]) for k in ("accepted_nodes", "bonus_token"))

@@ -65,6 +65,11 @@ def load():
     lib.tsv_noalloc_scratch_bytes.argtypes = []
     lib.tsv_kv_compact_accepted.restype = i32
     lib.tsv_kv_compact_accepted.argtypes = [P] * 7 + [i32] * 8 + [P, P]
+    lib.tsv_tree_reject_sample_ex.restype = i32
+    lib.tsv_tree_reject_sample_ex.argtypes = [P, P, P, P, P, P, f32, P, i32, i32, i32, P, P, P, P, P, P]
+    lib.tsv_tree_reject_sample_compact_ex.restype = i32
+    lib.tsv_tree_reject_sample_compact_ex.argtypes = ([P, P, P, P, P, P, f32, P, i32, i32, i32, P, P, P, P, P] +
+                                                      [P] * 5 + [i32] * 6 + [P, P])
     lib.tsv_tree_reject_sample_compact.restype = i32
     lib.tsv_tree_reject_sample_compact.argtypes = ([P, P, P, P, P, P, f32, i32, i32, i32, P, P, P, P, P] + [P] * 5 +
                                                    [i32] * 6 + [P, P])
@@ -148,32 +153,48 @@ def tree_verify_attn_noalloc(q, k_cache, v_cache, block_table, seq_lens, parent,
         _ptr(seq_err), _stream(stream)))
 
 
+class WalkOptions(ctypes.Structure):
+    """tsv_walk_options (include/tsv.h)."""
+    _fields_ = [("with_replacement", ctypes.c_int), ("logits_dtype", ctypes.c_int), ("top_k", ctypes.c_int),
+                ("top_p", ctypes.c_float)]
+
+
+def _walk_options(target_logits, with_replacement, top_k, top_p):
+    return WalkOptions(1 if with_replacement else 0, _dtype_code(target_logits), int(top_k), float(top_p))
+
+
 def tree_reject_sample(target_logits, draft_probs, draft_tokens, parent, u_accept, u_bonus,
                        temperature: float, accepted_nodes, accept_len, bonus_token, out_tokens, seq_err,
-                       stream=None):
-    """Rejection-sampling walk of the draft tree (see include/tsv.h)."""
+                       stream=None, with_replacement=False, top_k=0, top_p=1.0):
+    """Rejection-sampling walk of the draft tree (see include/tsv.h).  target_logits may
+    be float32 or bfloat16; with_replacement, top_k and top_p select the variants of
+    tsv_walk_options."""
     _contig(target_logits, draft_probs, draft_tokens, parent, u_accept, u_bonus, accepted_nodes, accept_len,
             bonus_token, out_tokens, seq_err)
     B, N, V = target_logits.shape
-    _check(load().tsv_tree_reject_sample(
+    opts = _walk_options(target_logits, with_replacement, top_k, top_p)
+    _check(load().tsv_tree_reject_sample_ex(
         _ptr(target_logits), _ptr(draft_probs), _ptr(draft_tokens), _ptr(parent), _ptr(u_accept), _ptr(u_bonus),
-        float(temperature), B, N, V, _ptr(accepted_nodes), _ptr(accept_len), _ptr(bonus_token), _ptr(out_tokens),
-        _ptr(seq_err), _stream(stream)))
+        float(temperature), ctypes.byref(opts), B, N, V, _ptr(accepted_nodes), _ptr(accept_len), _ptr(bonus_token),
+        _ptr(out_tokens), _ptr(seq_err), _stream(stream)))
 
 
 def tree_reject_sample_compact(target_logits, draft_probs, draft_tokens, parent, u_accept, u_bonus,
                                temperature: float, accepted_nodes, accept_len, bonus_token, out_tokens, seq_err,
-                               k_cache, v_cache, block_table, seq_lens, new_seq_lens, compact_err, stream=None):
+                               k_cache, v_cache, block_table, seq_lens, new_seq_lens, compact_err, stream=None,
+                               with_replacement=False, top_k=0, top_p=1.0):
     """The walk and the KV-cache rewrite of its accepted path in one launch (see include/tsv.h)."""
     _contig(target_logits, draft_probs, draft_tokens, parent, u_accept, u_bonus, accepted_nodes, accept_len,
             bonus_token, out_tokens, seq_err, k_cache, v_cache, block_table, seq_lens, new_seq_lens, compact_err)
     B, N, V = target_logits.shape
     num_blocks, bs, Hkv, D = k_cache.shape
-    _check(load().tsv_tree_reject_sample_compact(
+    opts = _walk_options(target_logits, with_replacement, top_k, top_p)
+    _check(load().tsv_tree_reject_sample_compact_ex(
         _ptr(target_logits), _ptr(draft_probs), _ptr(draft_tokens), _ptr(parent), _ptr(u_accept), _ptr(u_bonus),
-        float(temperature), B, N, V, _ptr(accepted_nodes), _ptr(accept_len), _ptr(bonus_token), _ptr(out_tokens),
-        _ptr(seq_err), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(new_seq_lens), Hkv, D,
-        bs, block_table.shape[1], num_blocks, _dtype_code(k_cache), _ptr(compact_err), _stream(stream)))
+        float(temperature), ctypes.byref(opts), B, N, V, _ptr(accepted_nodes), _ptr(accept_len), _ptr(bonus_token),
+        _ptr(out_tokens), _ptr(seq_err), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
+        _ptr(new_seq_lens), Hkv, D, bs, block_table.shape[1], num_blocks, _dtype_code(k_cache), _ptr(compact_err),
+        _stream(stream)))
 
 
 def kv_compact_accepted(k_cache, v_cache, block_table, seq_lens, accepted_nodes, accept_len, new_seq_lens,

@@ -168,10 +168,18 @@ tsv_status tsv_tree_verify_attn(const void* q, const void* k_cache, const void* 
 
 namespace {
 // Argument checks and packing shared by the walk alone and the walk with fused compaction.
-tsv_status reject_args(const float* target_logits, const float* draft_probs, const int32_t* draft_tokens,
+tsv_status reject_args(const void* target_logits, const float* draft_probs, const int32_t* draft_tokens,
                        const int32_t* parent, const float* u_accept, const float* u_bonus, float temperature, int B,
                        int N, int V, int32_t* accepted_nodes, int32_t* accept_len, int32_t* bonus_token,
-                       int32_t* out_tokens, int32_t* seq_err, tsv::SampleArgs* a) {
+                       int32_t* out_tokens, int32_t* seq_err, const tsv_walk_options* opts, tsv::SampleArgs* a) {
+    const tsv_walk_options o = opts ? *opts : tsv_walk_options{0, TSV_F32, 0, 1.0f};
+    if (o.with_replacement != 0 && o.with_replacement != 1)
+        return fail(TSV_ERR_ARG, "with_replacement must be 0 or 1, not %d", o.with_replacement);
+    if (o.logits_dtype != TSV_F32 && o.logits_dtype != TSV_BF16)
+        return fail(TSV_ERR_ARG, "bad logits dtype %d", (int)o.logits_dtype);
+    if (o.top_k < 0 || !(o.top_p > 0.0f && o.top_p <= 1.0f))
+        return fail(TSV_ERR_ARG, "top_k must be >= 0 and top_p in (0, 1]");
+    if (o.top_k > 0 || o.top_p < 1.0f) return fail(TSV_ERR_UNSUPPORTED, "top-k / top-p filtering is not built");
     if (B < 0 || N < 1 || V < 1) return fail(TSV_ERR_ARG, "bad sizes B=%d N=%d V=%d", B, N, V);
     if (N > tsv::kMaxNodes) return fail(TSV_ERR_UNSUPPORTED, "N=%d exceeds %d tree nodes", N, tsv::kMaxNodes);
     if (V > 16 * 512 * 32) return fail(TSV_ERR_UNSUPPORTED, "V=%d exceeds %d", V, 16 * 512 * 32);
@@ -190,6 +198,8 @@ tsv_status reject_args(const float* target_logits, const float* draft_probs, con
     a->u_accept = u_accept;
     a->u_bonus = u_bonus;
     a->T = temperature;
+    a->replacement = o.with_replacement;
+    a->logits_bf16 = o.logits_dtype == TSV_BF16;
     a->N = N;
     a->V = V;
     a->accepted_nodes = accepted_nodes;
@@ -218,18 +228,28 @@ tsv_status compact_args(void* k_cache, void* v_cache, const int32_t* block_table
 
 extern "C" {
 
+tsv_status tsv_tree_reject_sample_ex(const void* target_logits, const float* draft_probs,
+                                     const int32_t* draft_tokens, const int32_t* parent, const float* u_accept,
+                                     const float* u_bonus, float temperature, const tsv_walk_options* opts, int B,
+                                     int N, int V, int32_t* accepted_nodes, int32_t* accept_len,
+                                     int32_t* bonus_token, int32_t* out_tokens, int32_t* seq_err, void* stream) {
+    tsv::SampleArgs a;
+    const tsv_status st = reject_args(target_logits, draft_probs, draft_tokens, parent, u_accept, u_bonus, temperature,
+                                      B, N, V, accepted_nodes, accept_len, bonus_token, out_tokens, seq_err, opts, &a);
+    if (st != TSV_OK || B == 0) return st;
+    cudaError_t e = tsv::launch_tree_reject(a, B, device_sms(), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tree_reject_sample launch");
+    return TSV_OK;
+}
+
 tsv_status tsv_tree_reject_sample(const float* target_logits, const float* draft_probs,
                                   const int32_t* draft_tokens, const int32_t* parent, const float* u_accept,
                                   const float* u_bonus, float temperature, int B, int N, int V,
                                   int32_t* accepted_nodes, int32_t* accept_len, int32_t* bonus_token,
                                   int32_t* out_tokens, int32_t* seq_err, void* stream) {
-    tsv::SampleArgs a;
-    const tsv_status st = reject_args(target_logits, draft_probs, draft_tokens, parent, u_accept, u_bonus, temperature,
-                                      B, N, V, accepted_nodes, accept_len, bonus_token, out_tokens, seq_err, &a);
-    if (st != TSV_OK || B == 0) return st;
-    cudaError_t e = tsv::launch_tree_reject(a, B, device_sms(), static_cast<cudaStream_t>(stream));
-    if (e != cudaSuccess) return cuda_fail(e, "tree_reject_sample launch");
-    return TSV_OK;
+    return tsv_tree_reject_sample_ex(target_logits, draft_probs, draft_tokens, parent, u_accept, u_bonus, temperature,
+                                     nullptr, B, N, V, accepted_nodes, accept_len, bonus_token, out_tokens, seq_err,
+                                     stream);
 }
 
 tsv_status tsv_tree_reject_sample_compact(const float* target_logits, const float* draft_probs,
@@ -240,9 +260,25 @@ tsv_status tsv_tree_reject_sample_compact(const float* target_logits, const floa
                                           const int32_t* block_table, const int32_t* seq_lens,
                                           int32_t* new_seq_lens, int Hkv, int D, int block_size, int max_blocks,
                                           int num_blocks, tsv_dtype dtype, int32_t* compact_err, void* stream) {
+    return tsv_tree_reject_sample_compact_ex(target_logits, draft_probs, draft_tokens, parent, u_accept, u_bonus,
+                                             temperature, nullptr, B, N, V, accepted_nodes, accept_len, bonus_token,
+                                             out_tokens, seq_err, k_cache, v_cache, block_table, seq_lens,
+                                             new_seq_lens, Hkv, D, block_size, max_blocks, num_blocks, dtype,
+                                             compact_err, stream);
+}
+
+tsv_status tsv_tree_reject_sample_compact_ex(const void* target_logits, const float* draft_probs,
+                                             const int32_t* draft_tokens, const int32_t* parent,
+                                             const float* u_accept, const float* u_bonus, float temperature,
+                                             const tsv_walk_options* opts, int B, int N, int V,
+                                             int32_t* accepted_nodes, int32_t* accept_len, int32_t* bonus_token,
+                                             int32_t* out_tokens, int32_t* seq_err, void* k_cache, void* v_cache,
+                                             const int32_t* block_table, const int32_t* seq_lens,
+                                             int32_t* new_seq_lens, int Hkv, int D, int block_size, int max_blocks,
+                                             int num_blocks, tsv_dtype dtype, int32_t* compact_err, void* stream) {
     tsv::SampleArgs a;
     tsv_status st = reject_args(target_logits, draft_probs, draft_tokens, parent, u_accept, u_bonus, temperature, B,
-                                N, V, accepted_nodes, accept_len, bonus_token, out_tokens, seq_err, &a);
+                                N, V, accepted_nodes, accept_len, bonus_token, out_tokens, seq_err, opts, &a);
     if (st != TSV_OK) return st;
     st = compact_args(k_cache, v_cache, block_table, seq_lens, new_seq_lens, B, N, Hkv, D, block_size, max_blocks,
                       num_blocks, dtype, compact_err);

@@ -35,6 +35,7 @@
 // rejection, so a test is a comparison and a rejection costs one pass and one
 // cluster reduction whatever the number of earlier rejections.
 #include <cooperative_groups.h>
+#include <cuda_bf16.h>
 
 #include <map>
 #include <mutex>
@@ -161,24 +162,40 @@ __device__ __forceinline__ bool is_rejected(int v, int j, const int* xr) {
 
 __device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
-template <int VEC, bool ALIGNED>
-__device__ __forceinline__ void load_slice(const float* row, int v0, int v1, float (&x)[VEC][4], float fill) {
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+// four consecutive logits starting at a 4-entry boundary: one 16-byte (fp32) or
+// 8-byte (bf16) load
+__device__ __forceinline__ void load4_aligned(const float* p, float (&x)[4]) {
+    const float4 t = __ldg(reinterpret_cast<const float4*>(p));
+    x[0] = t.x;
+    x[1] = t.y;
+    x[2] = t.z;
+    x[3] = t.w;
+}
+__device__ __forceinline__ void load4_aligned(const __nv_bfloat16* p, float (&x)[4]) {
+    const uint2 t = __ldg(reinterpret_cast<const uint2*>(p));
+    x[0] = __uint_as_float(t.x << 16);  // a bf16 value is the top half of the float
+    x[1] = __uint_as_float(t.x & 0xffff0000u);
+    x[2] = __uint_as_float(t.y << 16);
+    x[3] = __uint_as_float(t.y & 0xffff0000u);
+}
+
+template <int VEC, bool ALIGNED, typename TL>
+__device__ __forceinline__ void load_slice(const TL* row, int v0, int v1, float (&x)[VEC][4], float fill) {
 #pragma unroll
     for (int k = 0; k < VEC; ++k) {
         const int base = v0 + (k * (int)blockDim.x + (int)threadIdx.x) * 4;
         if (ALIGNED) {
             if (base < v1) {
-                const float4 t = __ldg(reinterpret_cast<const float4*>(row + base));
-                x[k][0] = t.x;
-                x[k][1] = t.y;
-                x[k][2] = t.z;
-                x[k][3] = t.w;
+                load4_aligned(row + base, x[k]);
             } else {
                 x[k][0] = x[k][1] = x[k][2] = x[k][3] = fill;
             }
         } else {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) x[k][e] = (base + e < v1) ? __ldg(row + base + e) : fill;
+            for (int e = 0; e < 4; ++e) x[k][e] = (base + e < v1) ? to_f32(row[base + e]) : fill;
         }
     }
 }
@@ -219,13 +236,13 @@ __device__ __forceinline__ uint32_t owned_mask(const int* xr, int n, int v0, int
     return m;
 }
 
-template <int VEC>
-__device__ __forceinline__ void prefetch_slice(const float* row, int v0, int v1) {
+template <int VEC, typename TL>
+__device__ __forceinline__ void prefetch_slice(const TL* row, int v0, int v1) {
 #pragma unroll
     for (int k = 0; k < VEC; ++k) {
         const int base = v0 + (k * (int)blockDim.x + (int)threadIdx.x) * 4;
-        // one prefetch per 128-byte line: the thread whose float4 starts the line
-        if (base < v1 && ((reinterpret_cast<uintptr_t>(row + base) & 127) < 16)) prefetch_l2(row + base);
+        // one prefetch per 128-byte line: the thread whose four entries start the line
+        if (base < v1 && ((reinterpret_cast<uintptr_t>(row + base) & 127) < 4 * sizeof(TL))) prefetch_l2(row + base);
     }
 }
 
@@ -304,10 +321,11 @@ __device__ __forceinline__ void cluster_allreduce(cg::cluster_group& cluster, Re
 // Recomputes the normalised p of residual level `level` into the register slice from
 // the logits row and the recorded levels (the slow, per-entry chain; used only when a
 // residual sum is exactly zero).
-template <int VEC, bool ALIGNED>
-__device__ __forceinline__ void rebuild_level(float (&lv)[VEC][4], const float* lrow, const float* qrow, int v0, int v1,
+template <int VEC, bool ALIGNED, typename TL>
+__device__ __forceinline__ void rebuild_level(float (&lv)[VEC][4], const TL* lrow, const float* qrow, int v0, int v1,
                                            int level, float c2, float MC, float invZ, const int* xrej,
-                                           const float* inv_sq, const float* inv_zr, const int* zr_ok) {
+                                           const float* inv_sq, const float* inv_zr, const int* zr_ok,
+                                           bool replacement) {
     load_slice<VEC, ALIGNED>(lrow, v0, v1, lv, -INFINITY);
 #pragma unroll
     for (int k = 0; k < VEC; ++k) {
@@ -319,7 +337,8 @@ __device__ __forceinline__ void rebuild_level(float (&lv)[VEC][4], const float* 
             const int v = base + e;
             float p = ex2(fmaf(lv[k][e], c2, -MC)) * invZ;
             for (int j = 1; j <= level; ++j) {
-                const float qprev = (j == 1) ? qk[e] : (is_rejected(v, j - 1, xrej) ? 0.0f : qk[e] * inv_sq[j - 1]);
+                const float qprev = (j == 1 || replacement) ? qk[e]
+                                                            : (is_rejected(v, j - 1, xrej) ? 0.0f : qk[e] * inv_sq[j - 1]);
                 if (zr_ok[j]) p = fmaxf(0.0f, p - qprev) * inv_zr[j];
             }
             lv[k][e] = (v < v1) ? p : 0.0f;
@@ -343,7 +362,7 @@ __device__ __forceinline__ void fused_compact(const SampleArgs& a, int b, int A,
     }
 }
 
-template <int VEC, bool ALIGNED>
+template <int VEC, bool ALIGNED, typename TL>
 __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a) {
     pdl_wait();  // the inputs may come from the previous kernel in the stream
     pdl_launch_dependents();
@@ -424,7 +443,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
     int amax = 0;
 
     while (!err) {
-        const float* lrow = a.logits + ((long long)b * N + node) * V;
+        const TL* lrow = static_cast<const TL*>(a.logits) + ((long long)b * N + node) * V;
         const float* qrow = greedy ? nullptr : a.probs + ((long long)b * N + node) * V;
         // children of `node`, in index order (warp 0, by ballot)
         if (warp == 0) {
@@ -447,7 +466,10 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                 const int x = s_tok[s_kids[t]];
                 s_qx[t] = 0.0f;
                 if (x >= 0 && x < V) {
-                    cp_async4(&s_lx[t], lrow + x);
+                    if (sizeof(TL) == 4)
+                        cp_async4(&s_lx[t], lrow + x);
+                    else
+                        s_lx[t] = to_f32(lrow[x]);  // 2-byte entries: a plain load
                     if (!greedy) {
                         cp_async4(&s_qx[t], qrow + x);
                         cp_async4(&s_ux[t], a.u_accept + (long long)b * N + s_kids[t]);
@@ -458,7 +480,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
         }
         load_slice<VEC, ALIGNED>(lrow, v0, v1, lv, -INFINITY);
         // the first child's logits row into L2, for the likely case that it is accepted
-        if (nk > 0) prefetch_slice<VEC>(a.logits + ((long long)b * N + s_kids[0]) * V, v0, v1);
+        if (nk > 0) prefetch_slice<VEC>(static_cast<const TL*>(a.logits) + ((long long)b * N + s_kids[0]) * V, v0, v1);
 
         int bad = 0;
 #pragma unroll
@@ -614,8 +636,11 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
             }
             // rejected: residual sum at the next level (and, the first time, sum q)
             int qb = 0;
-            const uint32_t excl = owned_mask<VEC>(s_xrej, nrej, v0, v1);  // tokens out of q at this level
-            const float inv_sq = nrej > 0 ? s_inv_sq[nrej] : 1.0f;
+            // q at this level: the raw row at the node's first pass, and throughout when
+            // siblings were drafted independently (with replacement q is never updated)
+            const bool raw_q = nrej == 0 || a.replacement;
+            const uint32_t excl = raw_q ? 0u : owned_mask<VEC>(s_xrej, nrej, v0, v1);  // tokens out of q here
+            const float inv_sq = raw_q ? 1.0f : s_inv_sq[nrej];
             float zr = 0.0f, qs = 0.0f;
             constexpr int QG = VEC < 4 ? VEC : 4;  // draft entries loaded per group of vector steps
 #pragma unroll
@@ -648,7 +673,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                         if (v < v1 && !isfinite(q)) qb = 1;
                         // p and q at the current level
                         const float p = lv_is_p ? lv[k][e] * pscale : ex2(fmaf(lv[k][e], c2, -MC)) * invZf;
-                        const float qc = (nrej == 0) ? q : (((excl >> (k * 4 + e)) & 1u) ? 0.0f : q * inv_sq);
+                        const float qc = raw_q ? q : (((excl >> (k * 4 + e)) & 1u) ? 0.0f : q * inv_sq);
                         const float d = fmaxf(0.0f, p - qc);
                         zr += d;
                         qs += q;
@@ -716,7 +741,8 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                     int rf = s_rflag[t2];
                     if (s_tok[s_kids[t2]] == x) rf = 1;
                     s_px[t2] = p2;
-                    s_qc[t2] = (rf || !ff_pos(sq)) ? ff_make(0.0f) : ff_mul_f(inv_sq, s_qx[t2]);
+                    if (!a.replacement)  // with replacement the later children keep the raw q(x)
+                        s_qc[t2] = (rf || !ff_pos(sq)) ? ff_make(0.0f) : ff_mul_f(inv_sq, s_qx[t2]);
                     s_rflag[t2] = rf;
                 }
             }
@@ -729,7 +755,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                 // empty residual: p keeps its previous value, which the pass overwrote --
                 // rebuild it from the logits (unreachable in exact arithmetic)
                 rebuild_level<VEC, ALIGNED>(lv, lrow, qrow, v0, v1, nrej, c2, MC, invZf, s_xrej, s_inv_sq, s_inv_zr,
-                                            s_zr_ok);
+                                            s_zr_ok, a.replacement != 0);
                 lv_is_p = true;
                 pscale = 1.0f;
             }
@@ -966,14 +992,14 @@ static size_t reject_smem(int vpc) {
     return ALIGNED ? (size_t)vpc * sizeof(float) : 0;
 }
 
-template <int VEC, bool ALIGNED>
+template <int VEC, bool ALIGNED, typename TL>
 static cudaError_t make_reject_config(int B, int cs, int threads, int vpc, cudaStream_t stream,
                                       cudaLaunchConfig_t* cfg, cudaLaunchAttribute* attr) {
-    cudaError_t e = cudaFuncSetAttribute(tree_reject_kernel<VEC, ALIGNED>,
+    cudaError_t e = cudaFuncSetAttribute(tree_reject_kernel<VEC, ALIGNED, TL>,
                                          cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e != cudaSuccess) return e;
     const size_t smem = reject_smem<ALIGNED>(vpc);
-    e = cudaFuncSetAttribute(tree_reject_kernel<VEC, ALIGNED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(tree_reject_kernel<VEC, ALIGNED, TL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     *cfg = cudaLaunchConfig_t{};
@@ -990,18 +1016,18 @@ static cudaError_t make_reject_config(int B, int cs, int threads, int vpc, cudaS
     return cudaSuccess;
 }
 
-template <int VEC, bool ALIGNED>
+template <int VEC, bool ALIGNED, typename TL>
 static cudaError_t launch_reject_inst(const SampleArgs& a, int B, int cs, int threads, cudaStream_t stream) {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
-    cudaError_t e = make_reject_config<VEC, ALIGNED>(B, cs, threads, a.v_per_cta, stream, &cfg, attr);
+    cudaError_t e = make_reject_config<VEC, ALIGNED, TL>(B, cs, threads, a.v_per_cta, stream, &cfg, attr);
     if (e != cudaSuccess) return e;
-    return launch_pdl(tree_reject_kernel<VEC, ALIGNED>, cfg.gridDim, cfg.blockDim, cfg.dynamicSmemBytes, stream,
+    return launch_pdl(tree_reject_kernel<VEC, ALIGNED, TL>, cfg.gridDim, cfg.blockDim, cfg.dynamicSmemBytes, stream,
                       static_cast<unsigned>(cs), a);
 }
 
 // How many clusters of this shape can be resident at once (cached per shape).
-template <int VEC, bool ALIGNED>
+template <int VEC, bool ALIGNED, typename TL>
 static int resident_clusters(int cs, int threads, int vpc) {
     static std::mutex mu;
     static std::map<std::pair<long long, int>, int> cache;
@@ -1014,8 +1040,8 @@ static int resident_clusters(int cs, int threads, int vpc) {
     cudaLaunchConfig_t cfg;
     cudaLaunchAttribute attr[1];
     int n = 0;
-    if (make_reject_config<VEC, ALIGNED>(1, cs, threads, vpc, nullptr, &cfg, attr) != cudaSuccess ||
-        cudaOccupancyMaxActiveClusters(&n, tree_reject_kernel<VEC, ALIGNED>, &cfg) != cudaSuccess)
+    if (make_reject_config<VEC, ALIGNED, TL>(1, cs, threads, vpc, nullptr, &cfg, attr) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, tree_reject_kernel<VEC, ALIGNED, TL>, &cfg) != cudaSuccess)
         n = 0;
     cache[key] = n;
     return n;
@@ -1029,28 +1055,40 @@ static int vec_for(int V, int cs, int threads, int* vpc_out) {
     return need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : need <= 8 ? 8 : 0;
 }
 
-template <bool ALIGNED>
+template <bool ALIGNED, typename TL>
 static int resident_for(int vec, int cs, int threads, int vpc) {
     switch (vec) {
-        case 1: return resident_clusters<1, ALIGNED>(cs, threads, vpc);
-        case 2: return resident_clusters<2, ALIGNED>(cs, threads, vpc);
-        case 4: return resident_clusters<4, ALIGNED>(cs, threads, vpc);
-        default: return resident_clusters<8, ALIGNED>(cs, threads, vpc);
+        case 1: return resident_clusters<1, ALIGNED, TL>(cs, threads, vpc);
+        case 2: return resident_clusters<2, ALIGNED, TL>(cs, threads, vpc);
+        case 4: return resident_clusters<4, ALIGNED, TL>(cs, threads, vpc);
+        default: return resident_clusters<8, ALIGNED, TL>(cs, threads, vpc);
+    }
+}
+
+template <bool ALIGNED, typename TL>
+static cudaError_t launch_vec(const SampleArgs& a, int vec, int B, int cs, int threads, cudaStream_t stream) {
+    switch (vec) {
+        case 1: return launch_reject_inst<1, ALIGNED, TL>(a, B, cs, threads, stream);
+        case 2: return launch_reject_inst<2, ALIGNED, TL>(a, B, cs, threads, stream);
+        case 4: return launch_reject_inst<4, ALIGNED, TL>(a, B, cs, threads, stream);
+        case 8: return launch_reject_inst<8, ALIGNED, TL>(a, B, cs, threads, stream);
+        default: return cudaErrorInvalidValue;
     }
 }
 
 // Chooses the cluster size, block size and per-thread vector count for a vocabulary of
 // V entries and B sequences, then launches one cluster per sequence (16-CTA clusters
 // need 16 free SMs in one GPC, so their residency is checked).
-cudaError_t launch_tree_reject(SampleArgs a, int B, int num_sms, cudaStream_t stream) {
-    if (B == 0) return cudaSuccess;
+template <typename TL>
+static cudaError_t launch_tree_reject_t(SampleArgs a, int B, int num_sms, cudaStream_t stream) {
     const int V = a.V;
     int threads = 64;
     while (threads < 512 && threads * 4 * 2 < V) threads *= 2;
     const int cap1 = threads * 4 * 8;  // entries one CTA holds at VEC = 8
     int cs_min = 1;
     while (cs_min * cap1 < V) cs_min *= 2;  // smallest cluster that fits the row
-    const bool aligned = (V % 4) == 0 && (reinterpret_cast<uintptr_t>(a.logits) & 15) == 0 &&
+    // aligned: four entries per vector load start on a 16-byte (fp32) / 8-byte (bf16) boundary
+    const bool aligned = (V % 4) == 0 && (reinterpret_cast<uintptr_t>(a.logits) & (4 * sizeof(TL) - 1)) == 0 &&
                          (a.probs == nullptr || (reinterpret_cast<uintptr_t>(a.probs) & 15) == 0);
     // Enough CTAs that a thread holds at most 8 entries: every visited node costs a
     // pass over the slice, and the slice load dominates it.  A cluster larger than the
@@ -1063,23 +1101,21 @@ cudaError_t launch_tree_reject(SampleArgs a, int B, int num_sms, cudaStream_t st
         int vpc;
         const int vec = vec_for(V, cs, threads, &vpc);
         if (vec == 0) continue;
-        const int res = aligned ? resident_for<true>(vec, cs, threads, vpc) : resident_for<false>(vec, cs, threads, vpc);
+        const int res =
+            aligned ? resident_for<true, TL>(vec, cs, threads, vpc) : resident_for<false, TL>(vec, cs, threads, vpc);
         if (res >= B && B * cs <= num_sms) break;
     }
     int vpc;
     const int vec = vec_for(V, cs, threads, &vpc);
     a.v_per_cta = vpc;
-    switch (vec) {
-        case 1: return aligned ? launch_reject_inst<1, true>(a, B, cs, threads, stream)
-                               : launch_reject_inst<1, false>(a, B, cs, threads, stream);
-        case 2: return aligned ? launch_reject_inst<2, true>(a, B, cs, threads, stream)
-                               : launch_reject_inst<2, false>(a, B, cs, threads, stream);
-        case 4: return aligned ? launch_reject_inst<4, true>(a, B, cs, threads, stream)
-                               : launch_reject_inst<4, false>(a, B, cs, threads, stream);
-        case 8: return aligned ? launch_reject_inst<8, true>(a, B, cs, threads, stream)
-                               : launch_reject_inst<8, false>(a, B, cs, threads, stream);
-        default: return cudaErrorInvalidValue;
-    }
+    return aligned ? launch_vec<true, TL>(a, vec, B, cs, threads, stream)
+                   : launch_vec<false, TL>(a, vec, B, cs, threads, stream);
+}
+
+cudaError_t launch_tree_reject(SampleArgs a, int B, int num_sms, cudaStream_t stream) {
+    if (B == 0) return cudaSuccess;
+    return a.logits_bf16 ? launch_tree_reject_t<__nv_bfloat16>(a, B, num_sms, stream)
+                         : launch_tree_reject_t<float>(a, B, num_sms, stream);
 }
 
 }  // namespace tsv

@@ -7,13 +7,15 @@
 namespace tsv {
 
 struct SampleArgs {
-    const float* logits;
+    const void* logits;  // [B, N, V] fp32, or bf16 when logits_bf16
     const float* probs;
     const int32_t* tokens;
     const int32_t* parent;
     const float* u_accept;
     const float* u_bonus;
     float T;
+    int replacement;  // siblings drafted independently from q (with replacement): q is never updated
+    int logits_bf16;
     int N;
     int V;
     int v_per_cta;  // vocabulary entries owned by one CTA (multiple of 4); set by the launcher

@@ -52,6 +52,7 @@ class Workload:
     depth: int = 0  # depth cap for "random" trees
     branching: tuple = ()  # per-level children for "topk" trees
     pq_frac: float = 0.0  # fraction of sequences whose target logits equal the draft logits
+    siblings: str = "without"  # "without": siblings drafted without replacement; "independent": i.i.d. from q
     seed: int = 1000
     block_size: int = BLOCK_SIZE
 
@@ -316,8 +317,9 @@ def generate(w: Workload, *, seed: Optional[int] = None, temperature: Optional[f
         target_logits[pq_seqs] = draft_logits[pq_seqs]
 
     # 7. draft tokens: the children of node i are drafted from node i's draft
-    #    distribution without replacement (Gumbel-top-k), in child-index order; at
-    #    T == 0 they are the top-k of the draft logits.  The root's own token is the
+    #    distribution without replacement (Gumbel-top-k), in child-index order, or
+    #    independently (siblings="independent"); at T == 0 they are the top-k of the
+    #    draft logits.  The root's own token is the
     #    last accepted token and is drawn uniformly.
     draft_tokens = np.zeros((B, N), dtype=np.int32)
     draft_tokens[:, 0] = rng.integers(0, V, size=B)
@@ -331,6 +333,12 @@ def generate(w: Workload, *, seed: Optional[int] = None, temperature: Optional[f
             k = len(kids[i])
             if k > V:
                 raise ValueError(f"node {i} has {k} children but the vocabulary has only {V} tokens")
+            if T > 0 and w.siblings == "independent":
+                # each child drawn independently from q (inverse CDF of one uniform each)
+                cdf = np.cumsum(draft_probs[b, i].astype(np.float64))
+                u = rng.random(k) * cdf[-1]
+                draft_tokens[b, kids[i]] = np.minimum(np.searchsorted(cdf, u, side="right"), V - 1)
+                continue
             if T > 0:
                 key = np.log(draft_probs[b, i].astype(np.float64)) + rng.gumbel(size=V)
             else:
