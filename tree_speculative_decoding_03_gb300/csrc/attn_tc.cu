@@ -187,6 +187,40 @@ __device__ __forceinline__ float ex2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// three-input maximum (one instruction on sm_100 and later)
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+// packed pairs of fp32 (one instruction per pair on sm_100 and later)
+__device__ __forceinline__ unsigned long long f2_pack(float lo, float hi) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(unsigned long long r, float& lo, float& hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// register budget per thread after the set-up: the producer / MMA warpgroup gives up
+// registers, the softmax warpgroups (which hold a whole 128-key S row) take them:
+// 128 x 96 + 256 x 200 <= 384 x 168, the registers the CTA is launched with
+template <uint32_t R>
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(R)); }
+template <uint32_t R>
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(R)); }
+constexpr uint32_t kRegsProducer = 96, kRegsSoftmax = 200;
+static_assert(128 * kRegsProducer + 256 * kRegsSoftmax <= 384 * 168, "register split exceeds the launch");
 
 // Shared-memory matrix descriptor, 128B swizzle, version 1 (tcgen05).
 // lbo/sbo in bytes: K-major tiles use sbo = 1024 (8 rows x 128B) and no lbo; MN-major
@@ -461,6 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int my_err = 0;
     int err_b = it0.b;  // sequence flagged if a wait of this thread gives up
 
+    if (warp < 4) regs_dec<kRegsProducer>();  // warpgroup 0: producer, MMA issuer, two idle warps
     if (warp == 0) {
         // ============================ TMA producer (whole warp: lane j loads the id of
         // the tile's j-th cache block and issues that block's boxes).  The next tile's
@@ -523,24 +558,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idO = idesc_bf16(128, D, true);
             const uint32_t q_base = smem_u32(smem + lay.q0);
             const uint32_t ring_base = smem_u32(smem + lay.ring);
+            // The descriptors are built once: a descriptor's start-address field is the
+            // byte address >> 4 in its low bits, so the descriptor of (base + off) is the
+            // base descriptor + off / 16 (every offset here is a multiple of 16 and all
+            // addresses stay below 2^18).  Each MMA then costs one 64-bit add per operand.
+            const uint64_t dQ = sdesc_sw128(q_base, 16, 1024);       // K-major Q tiles
+            const uint64_t dK = sdesc_sw128(ring_base, 16, 1024);    // K-major K tiles
+            const uint64_t dV = sdesc_sw128(ring_base, kHalfBytes, 1024);  // MN-major V tiles
             // S buffer sb (TMEM columns sb*128) = Q tile qm . K^T
             auto issue_S = [=](int qm, int sb, int slot) {
-                const uint32_t qa = q_base + qm * (128u * D * 2u);
-                const uint32_t kb = ring_base + slot * SLOT;
+                const uint64_t qa = dQ + ((qm * (128u * D * 2u)) >> 4);
+                const uint64_t kb = dK + ((slot * SLOT) >> 4);
+                const uint32_t d = tmem + sb * 128;
 #pragma unroll
                 for (int k = 0; k < D / 16; ++k) {
-                    const uint32_t off = (k >> 2) * kHalfBytes + (k & 3) * 32;
-                    mma_bf16(tmem + sb * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idS,
-                             k > 0);
+                    const uint32_t off16 = ((k >> 2) * kHalfBytes + (k & 3) * 32) >> 4;
+                    mma_bf16(d, qa + off16, kb + off16, idS, k > 0);
                 }
             };
             // O tile om += P . V, P in TMEM over S buffer pb's columns (16 keys = 8 columns per MMA)
             auto issue_PV = [=](int om, int pb, int slot, bool acc_first) {
-                const uint32_t vb = ring_base + slot * SLOT;
+                const uint64_t vb = dV + ((slot * SLOT) >> 4);
+                const uint32_t d = tmem + 256 + om * D, pa = tmem + pb * 128;
 #pragma unroll
                 for (int k = 0; k < kTileKeys / 16; ++k)
-                    mma_bf16_ts(tmem + 256 + om * D, tmem + pb * 128 + k * 8,
-                                sdesc_sw128(vb + k * 16 * 128, kHalfBytes, 1024), idO, (acc_first || k > 0) ? 1u : 0u);
+                    mma_bf16_ts(d, pa + k * 8, vb + ((k * 16 * 128) >> 4), idO, (acc_first || k > 0) ? 1u : 0u);
             };
             // K tile of CTA tile jt in its slot; a tile that starts a segment also waits
             // for that segment's Q.  *first = the tile starts a segment.
@@ -638,7 +680,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             volatile int never = 0;
             if (!mbar_wait(bar(Bars::kDone), 0, &never)) my_err = 1;
         }
-    } else if (warp >= 4 && (warp - 4) / 4 < nm) {
+    } else if (warp >= 4) {
+        regs_inc<kRegsSoftmax>();  // both softmax warpgroups, also the second one when it has no M tile
+        if ((warp - 4) / 4 < nm) {
         // ============================ softmax warpgroups (warpgroup wg < nm)
         const int wg = (warp - 4) >> 2;
         const int nthr = 128 * nm;           // softmax threads taking part
@@ -754,51 +798,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (stid < N) par_next = __ldg(a.parent + (long long)nx.b * N + stid);
                 }
                 if (warp_active) {
-                    // Two passes over the S row in TMEM, 64 columns per wait: the raw max
-                    // first, then P = 2^(s*scale - m) written as bf16 pairs over the S
-                    // columns.  Independent accumulators (8 for the max, 4 for the sum) keep
-                    // the FMNMX/MUFU latency chains short.  A tile that reaches past the
-                    // prefix first sets its hidden scores to -inf (one visibility bit per
-                    // key) and stores them back, so both passes run the same code for
-                    // every tile.
-                    const bool full_tile = (t0 + kTileKeys <= L);
-                    uint32_t vis0 = 0xffffffffu, vis1 = 0xffffffffu, vis2 = 0xffffffffu, vis3 = 0xffffffffu;
-                    if (!full_tile) {
-                        vis0 = vis_word(t0 - L, anc0, anc1, anc2, anc3);
-                        vis1 = vis_word(t0 + 32 - L, anc0, anc1, anc2, anc3);
-                        vis2 = vis_word(t0 + 64 - L, anc0, anc1, anc2, anc3);
-                        vis3 = vis_word(t0 + 96 - L, anc0, anc1, anc2, anc3);
+                    // One pass over the S row: all 128 scores come out of TMEM under one wait
+                    // and stay in registers; keys off the row's path (a tile that reaches past
+                    // the prefix) become -inf there; the raw max by three-input maxima; then
+                    // P = 2^(s*scale - m) with the scale and offset applied to pairs of
+                    // scores at a time, summed in pairs, packed to bf16 pairs over the first
+                    // 64 columns.
+                    uint32_t sv[128];
+                    tmem_ld32(tS, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+                    tmem_ld32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+                    tmem_ld32(tS + 64, *reinterpret_cast<uint32_t(*)[32]>(&sv[64]));
+                    tmem_ld32(tS + 96, *reinterpret_cast<uint32_t(*)[32]>(&sv[96]));
+                    tmem_wait_ld();
+                    if (t0 + kTileKeys > L) {
+#pragma unroll
+                        for (int w4 = 0; w4 < 4; ++w4) {
+                            const uint32_t vw = vis_word(t0 + 32 * w4 - L, anc0, anc1, anc2, anc3);
+#pragma unroll
+                            for (int cc = 0; cc < 32; ++cc)
+                                sv[32 * w4 + cc] = ((vw >> cc) & 1u) ? sv[32 * w4 + cc] : 0xff800000u;  // -inf
+                        }
                     }
                     float mxa[8];
 #pragma unroll
                     for (int q = 0; q < 8; ++q) mxa[q] = -INFINITY;
-#pragma unroll 1
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        uint32_t pa[32], pb[32];
-                        tmem_ld32(tS + h2 * 64, pa);
-                        tmem_ld32(tS + h2 * 64 + 32, pb);
-                        tmem_wait_ld();
-                        if (!full_tile) {
-                            const uint32_t va = h2 ? vis2 : vis0, vb = h2 ? vis3 : vis1;
+                    if (valid) {
 #pragma unroll
-                            for (int cc = 0; cc < 32; ++cc) {
-                                pa[cc] = ((va >> cc) & 1u) ? pa[cc] : 0xff800000u;  // -inf
-                                pb[cc] = ((vb >> cc) & 1u) ? pb[cc] : 0xff800000u;
-                            }
-                            tmem_st32(tS + h2 * 64, pa);
-                            tmem_st32(tS + h2 * 64 + 32, pb);
-                            tmem_wait_st();
-                        }
-                        if (valid) {
+                        for (int cc = 0; cc < 128; cc += 16)
 #pragma unroll
-                            for (int cc = 0; cc < 32; ++cc) {
-                                mxa[cc & 7] = fmaxf(mxa[cc & 7], __uint_as_float(pa[cc]));
-                                mxa[cc & 7] = fmaxf(mxa[cc & 7], __uint_as_float(pb[cc]));
-                            }
-                        }
+                            for (int q = 0; q < 8; ++q)
+                                mxa[q] = max3f(mxa[q], __uint_as_float(sv[cc + 2 * q]), __uint_as_float(sv[cc + 2 * q + 1]));
                     }
-                    const float mx_raw = fmaxf(fmaxf(fmaxf(mxa[0], mxa[1]), fmaxf(mxa[2], mxa[3])),
-                                               fmaxf(fmaxf(mxa[4], mxa[5]), fmaxf(mxa[6], mxa[7])));
+                    const float mx_raw = max3f(max3f(mxa[0], mxa[1], mxa[2]), max3f(mxa[3], mxa[4], mxa[5]),
+                                               fmaxf(mxa[6], mxa[7]));
                     const float mx = mx_raw * sl2;  // scale > 0: max commutes with it
                     // within a segment, the PV product of the previous tile must be done
                     // before O is rescaled (a segment's first PV overwrites O)
@@ -830,40 +862,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tmem_wait_st();
                     }
                     const bool live = valid && m_run != -INFINITY;
-                    const float neg_m = -m_run;
-                    float la[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll 1
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        uint32_t pa[32], pb[32];
-                        tmem_ld32(tS + h2 * 64, pa);
-                        tmem_ld32(tS + h2 * 64 + 32, pb);
-                        tmem_wait_ld();
-                        // P in place of the scores (as bit patterns): pa = columns 0..31, pb =
-                        // 32..63; a hidden key's -inf score gives 2^-inf = 0
-                        if (live) {
+                    const unsigned long long sc2 = f2_pack(sl2, sl2), off2 = f2_pack(-m_run, -m_run);
+                    unsigned long long la2[4] = {0ull, 0ull, 0ull, 0ull};  // (0.0f, 0.0f) pairs
+                    uint32_t w[64];
 #pragma unroll
-                            for (int cc = 0; cc < 32; ++cc) {
-                                pa[cc] = __float_as_uint(ex2(fmaf(__uint_as_float(pa[cc]), sl2, neg_m)));
-                                pb[cc] = __float_as_uint(ex2(fmaf(__uint_as_float(pb[cc]), sl2, neg_m)));
-                            }
-                        } else {
-#pragma unroll
-                            for (int cc = 0; cc < 32; ++cc) pa[cc] = pb[cc] = 0u;
-                        }
-                        // pack to bf16 pairs and store over the S columns already read
-                        uint32_t w[32];
-#pragma unroll
-                        for (int q = 0; q < 32; ++q) {
-                            const float p0 = __uint_as_float(q < 16 ? pa[2 * q] : pb[2 * q - 32]);
-                            const float p1 = __uint_as_float(q < 16 ? pa[2 * q + 1] : pb[2 * q - 31]);
-                            la[q & 3] += p0 + p1;
-                            __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
-                            w[q] = *reinterpret_cast<uint32_t*>(&pk);
-                        }
-                        tmem_st32(tS + h2 * 32, w);
+                    for (int q = 0; q < 64; ++q) {
+                        // a hidden key's -inf score gives 2^-inf = 0
+                        float x0, x1;
+                        f2_unpack(f2_fma(f2_pack(__uint_as_float(sv[2 * q]), __uint_as_float(sv[2 * q + 1])), sc2, off2),
+                                  x0, x1);
+                        const float p0 = live ? ex2(x0) : 0.0f;
+                        const float p1 = live ? ex2(x1) : 0.0f;
+                        la2[q & 3] = f2_add(la2[q & 3], f2_pack(p0, p1));
+                        __nv_bfloat162 pk = __floats2bfloat162_rn(p0, p1);
+                        w[q] = *reinterpret_cast<uint32_t*>(&pk);
                     }
+                    tmem_st32(tS, *reinterpret_cast<uint32_t(*)[32]>(&w[0]));
+                    tmem_st32(tS + 32, *reinterpret_cast<uint32_t(*)[32]>(&w[32]));
                     tmem_wait_st();
-                    l_run += (la[0] + la[1]) + (la[2] + la[3]);
+                    float s0, s1, s2, s3, s4, s5, s6, s7;
+                    f2_unpack(la2[0], s0, s1);
+                    f2_unpack(la2[1], s2, s3);
+                    f2_unpack(la2[2], s4, s5);
+                    f2_unpack(la2[3], s6, s7);
+                    l_run += ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
                 }
                 // a unit's last tile: V rows past the key range are zeroed before the PV
                 // product (they may hold stale or foreign data; P is 0 there but 0 * NaN is NaN)
@@ -935,6 +957,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++seg;
         }
         if (!ok) my_err = 1;
+        }
     }
     // the check kernel has written seq_err before this CTA completes (and so before the
     // merge kernel runs, or a timeout flag is added to it)
