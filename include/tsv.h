@@ -195,8 +195,11 @@ tsv_status tsv_tree_reject_sample(const float *target_logits, const float *draft
  *   to its top_k most probable tokens (top_k = 0: all), then to the smallest prefix
  *   of them, by decreasing p with ties to the lower index, whose mass reaches top_p
  *   (top_p = 1: all), and renormalised; q is the drafter's own (filtered)
- *   distribution as given.  Not built yet: nonzero top_k or top_p < 1 return
- *   TSV_ERR_UNSUPPORTED.
+ *   distribution as given.  top_k >= V keeps every token.  The cut is found by
+ *   bisection over the logits' order (about 35 cluster reductions per visited node,
+ *   a few more when the boundary falls inside a run of equal logits), so a filtered
+ *   walk costs several times the plain one.  Mass sums are float-float; a cut whose
+ *   cumulative mass lies within ~1e-7 of top_p may differ from an exact computation.
  * ------------------------------------------------------------------------- */
 typedef struct {
     int with_replacement;

@@ -116,7 +116,8 @@ def tree_reject_sample(inp: dict, *, temperature: Optional[float] = None, mutant
     rc = _lib(mutant).oracle_tree_reject_sample(
         _ptr(logits), _ptr(probs), _ptr(tok), _ptr(par), _ptr(ua), _ptr(ub), T, B, N, V,
         _ptr(r["accepted_nodes"]), _ptr(r["accept_len"]), _ptr(r["bonus_token"]), _ptr(r["out_tokens"]),
-        _ptr(r["ratio"]), _ptr(r["bonus_cdf"]), _ptr(r["err"]), 1 if replacement else 0, int(top_k), float(top_p),
+        _ptr(r["ratio"]), _ptr(r["bonus_cdf"]), _ptr(r["err"]), 1 if replacement else 0, int(top_k),
+        float(np.float32(top_p)),  # the threshold as the library's float argument holds it
         DTYPE_CODE["bf16" if bf16_logits else "f32"])
     if rc != 0:
         raise ValueError("oracle_tree_reject_sample: bad arguments")

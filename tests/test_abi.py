@@ -54,7 +54,7 @@ def test_host_argument_checks_need_no_gpu(lib):
     ex = lib.tsv_tree_reject_sample_ex
     for opts, want in ((WalkOptions(2, 1, 0, 1.0), tsv.TSV_ERR_ARG), (WalkOptions(0, 7, 0, 1.0), tsv.TSV_ERR_ARG),
                        (WalkOptions(0, 1, -1, 1.0), tsv.TSV_ERR_ARG), (WalkOptions(0, 1, 0, 0.0), tsv.TSV_ERR_ARG),
-                       (WalkOptions(0, 1, 0, 1.5), tsv.TSV_ERR_ARG)):
+                       (WalkOptions(0, 1, 0, 1.5), tsv.TSV_ERR_ARG), (WalkOptions(0, 1, 0, float("nan")), tsv.TSV_ERR_ARG)):
         assert ex(*[16] * 6, 1.0, ctypes.byref(opts), 4, 8, 100, *[16] * 5, P) == want
     assert ex(*walk, 1.0, None, 0, 8, 100, *[P] * 5, P) == tsv.TSV_OK  # NULL options, empty batch
     # single-chunk plans need no workspace

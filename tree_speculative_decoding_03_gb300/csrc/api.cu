@@ -179,7 +179,6 @@ tsv_status reject_args(const void* target_logits, const float* draft_probs, cons
         return fail(TSV_ERR_ARG, "bad logits dtype %d", (int)o.logits_dtype);
     if (o.top_k < 0 || !(o.top_p > 0.0f && o.top_p <= 1.0f))
         return fail(TSV_ERR_ARG, "top_k must be >= 0 and top_p in (0, 1]");
-    if (o.top_k > 0 || o.top_p < 1.0f) return fail(TSV_ERR_UNSUPPORTED, "top-k / top-p filtering is not built");
     if (B < 0 || N < 1 || V < 1) return fail(TSV_ERR_ARG, "bad sizes B=%d N=%d V=%d", B, N, V);
     if (N > tsv::kMaxNodes) return fail(TSV_ERR_UNSUPPORTED, "N=%d exceeds %d tree nodes", N, tsv::kMaxNodes);
     if (V > 16 * 512 * 32) return fail(TSV_ERR_UNSUPPORTED, "V=%d exceeds %d", V, 16 * 512 * 32);
@@ -199,6 +198,8 @@ tsv_status reject_args(const void* target_logits, const float* draft_probs, cons
     a->u_bonus = u_bonus;
     a->T = temperature;
     a->replacement = o.with_replacement;
+    a->top_k = o.top_k;
+    a->top_p = o.top_p;
     a->logits_bf16 = o.logits_dtype == TSV_BF16;
     a->N = N;
     a->V = V;

@@ -346,6 +346,15 @@ __device__ __forceinline__ void rebuild_level(float (&lv)[VEC][4], const TL* lro
     }
 }
 
+// Order key of a logit: a larger float has a larger key (sign-magnitude to biased).
+__device__ __forceinline__ uint32_t order_key(float l) {
+    const uint32_t u = __float_as_uint(l);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float order_key_value(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7fffffffu) : ~key);
+}
+
 // Fused tail (rank 0 of the cluster, every thread): the KV-cache rewrite of the
 // accepted path, exactly as the compaction kernel does it; A < 0 (walk error) leaves
 // the sequence untouched.
@@ -406,8 +415,38 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
     float* s_q = reinterpret_cast<float*>(s_dyn);
     const bool bulk = ALIGNED && v1 > v0;
     const ff invT_ff = greedy ? ff_make(0.0f) : ff_div(ff_make(1.0f), ff_make(T));
+    // top-k / top-p filter of the target at every visited node (0 / 1: none)
+    const bool filtered = (a.top_k > 0 && a.top_k < V) || a.top_p < 1.0f;
+    const float kt = (a.top_k > 0 && a.top_k < V) ? (float)a.top_k : 3.0e38f;
 
     int parity = 0;
+    // Block then cluster sum of two per-thread fp32 values (float-float across warps and
+    // CTAs, combined in rank order): the results are in s_all (hi, lo) and (hi2, lo2).
+    // Called by every thread of every CTA.
+    auto reduce_sums = [&](float x, float y) {
+        x = warp_sum(x);
+        y = warp_sum(y);
+        if (lane == 0) {
+            s_wf[warp] = x;
+            s_wg[warp] = y;
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const ff z1 = warp_sum_ff(ff_make(lane < nwarps ? s_wf[lane] : 0.0f));
+            const ff z2 = warp_sum_ff(ff_make(lane < nwarps ? s_wg[lane] : 0.0f));
+            if (lane == 0) {
+                RedSlot r{};
+                r.hi = z1.hi;
+                r.lo = z1.lo;
+                r.hi2 = z2.hi;
+                r.lo2 = z2.lo;
+                s_cta = r;
+            }
+        }
+        __syncthreads();
+        cluster_allreduce(cluster, s_red, parity, s_cta, kRedSums, c2, &s_all);
+        parity ^= 1;
+    };
 
     // fused rewrite (rank 0): the last warp checks the sequence's cache blocks now, while
     // the walk runs, so the tail only checks the path and moves the rows
@@ -602,6 +641,115 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
         if (s_all.flag) {
             err = TSV_DERR_NONFINITE;
             break;
+        }
+        if (!greedy && filtered) {
+            // ---- top-k / top-p filtered target (Sequoia summary, "More on tables"): keep the
+            // first entries of the row in order of decreasing p (= decreasing logit; ties to
+            // the lower index) up to the first position where their number reaches top_k or
+            // their unfiltered mass reaches top_p; renormalise over them.  The boundary
+            // entry's order key is found bit by bit (every probe one cluster reduction of a
+            // count and a float-float mass, identical in every CTA), a partial run of equal
+            // logits at the boundary is cut by index the same way.
+            const ff pt = ff_make(a.top_p < 1.0f ? a.top_p : 3.0e38f);
+            auto cond = [&](float cnt, ff mass) { return cnt >= kt || !ff_lt(mass, pt); };
+            uint32_t theta = 0u;
+            for (int bit = 31; bit >= 0; --bit) {
+                const uint32_t cand = theta | (1u << bit);
+                float cn = 0.0f, ms = 0.0f;
+#pragma unroll
+                for (int k = 0; k < VEC; ++k)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int v = v0 + (k * (int)blockDim.x + tid) * 4 + e;
+                        if (v < v1 && order_key(lv[k][e]) >= cand) {
+                            cn += 1.0f;
+                            ms += ex2(fmaf(lv[k][e], c2, -MC)) * invZf;
+                        }
+                    }
+                reduce_sums(cn, ms);
+                if (cond(s_all.hi, ff{s_all.hi2, s_all.lo2})) theta = cand;
+            }
+            // entries above the boundary key, and the run of entries equal to it
+            float ca = 0.0f, ma = 0.0f, ct = 0.0f;
+#pragma unroll
+            for (int k = 0; k < VEC; ++k)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int v = v0 + (k * (int)blockDim.x + tid) * 4 + e;
+                    if (v >= v1) continue;
+                    const uint32_t key = order_key(lv[k][e]);
+                    if (key > theta) {
+                        ca += 1.0f;
+                        ma += ex2(fmaf(lv[k][e], c2, -MC)) * invZf;
+                    } else if (key == theta) {
+                        ct += 1.0f;
+                    }
+                }
+            reduce_sums(ca, ma);
+            const float c_above = s_all.hi;
+            const ff m_above{s_all.hi2, s_all.lo2};
+            reduce_sums(ct, 0.0f);
+            const int n_tie = (int)s_all.hi;
+            // how many of the tied entries the cut keeps (all CTAs compute the same)
+            const float p_tie = ex2(fmaf(order_key_value(theta), c2, -MC)) * invZf;
+            int keep_ties = n_tie;
+            if (a.top_k > 0) keep_ties = min(keep_ties, max(1, (int)(kt - c_above)));
+            if (a.top_p < 1.0f) {
+                int tp = 1;
+                while (tp < keep_ties && ff_lt(ff_add(m_above, ff_mul_f(ff_make((float)tp), p_tie)), pt)) ++tp;
+                keep_ties = min(keep_ties, tp);
+            }
+            int idx_end = V;  // tied entries with index < idx_end are kept
+            if (keep_ties < n_tie) {
+                // index of the keep_ties-th tied entry: the largest bound with fewer ties below it
+                int bound = 0;
+                for (int bit = 20; bit >= 0; --bit) {
+                    const int cand = bound | (1 << bit);
+                    float cn = 0.0f;
+#pragma unroll
+                    for (int k = 0; k < VEC; ++k)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const int v = v0 + (k * (int)blockDim.x + tid) * 4 + e;
+                            if (v < v1 && v < cand && order_key(lv[k][e]) == theta) cn += 1.0f;
+                        }
+                    reduce_sums(cn, 0.0f);
+                    if ((int)s_all.hi < keep_ties) bound = cand;
+                }
+                idx_end = bound + 1;
+            }
+            // drop the rest and renormalise over the kept entries
+            float zk = 0.0f;
+#pragma unroll
+            for (int k = 0; k < VEC; ++k)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int v = v0 + (k * (int)blockDim.x + tid) * 4 + e;
+                    const uint32_t key = order_key(lv[k][e]);
+                    const bool kept = v < v1 && (key > theta || (key == theta && v < idx_end));
+                    if (!kept) lv[k][e] = -INFINITY;
+                    else zk += ex2(fmaf(lv[k][e], c2, -MC));
+                }
+            reduce_sums(zk, 0.0f);
+            const ff zkeep{s_all.hi, s_all.lo};
+            invZf = 1.0f / ff_float(zkeep);
+            if (warp == 0) {  // the children's p(x) under the filtered target
+                const ff invZ = ff_recip(ff_mul_f(zkeep, exp2f(-fmaf(M, c2, -MC))));
+                for (int t = lane; t < nk; t += 32) {
+                    const int x = s_tok[s_kids[t]];
+                    const float lx = s_lx[t];
+                    const uint32_t key = order_key(lx);
+                    const bool kept = key > theta || (key == theta && x < idx_end);
+                    ff px = ff_make(0.0f);
+                    if (kept && isfinite(s_qx[t])) {
+                        const ff arg = ff_mul(two_sum(lx, -M), invT_ff);
+                        const float ex = expf(arg.hi);
+                        px = ff_mul(quick_two_sum(ex, ex * arg.lo), invZ);
+                    }
+                    s_px[t] = px;
+                }
+            }
+            __syncthreads();
         }
 
         // ---- children, in index order

@@ -15,6 +15,8 @@ struct SampleArgs {
     const float* u_bonus;
     float T;
     int replacement;  // siblings drafted independently from q (with replacement): q is never updated
+    int top_k;        // > 0: target filtered to its top_k tokens at every visited node
+    float top_p;      // < 1: target filtered to the smallest top set of mass >= top_p
     int logits_bf16;
     int N;
     int V;
