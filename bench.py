@@ -2,8 +2,9 @@
 """Benchmark of one tree-verification step on GB300.
 
 A step is one pass of the whole hot path over one synthetic batch, on one CUDA
-stream: tsv_tree_verify_attn (sequence checks, tree-masked attention over a
-persistent even split of all K/V tiles, merge of split units) and
+stream: tsv_tree_verify_attn_append (sequence checks with the tree's new K/V rows
+written into the paged cache, tree-masked attention over a persistent even split of
+all K/V tiles, merge of split units) and
 tsv_tree_reject_sample_compact (rejection-sampling walk + bonus token, with the KV
 rewrite of the accepted path in the same launch).
 
@@ -169,12 +170,23 @@ def whole_job_rate(units_per_rank: float, seconds: float, world: int) -> float:
 
 # ----------------------------------------------------------------------------- algorithmic work
 
-def attn_bytes(inp):
-    """K/V of every visible slot (prefix + tree) once, plus Q in and O out."""
+def attn_bytes(inp, append=True):
+    """K/V of every visible slot (prefix + tree) once, plus Q in and O out; with the
+    fused append also the tree's new K/V rows read and written into the cache."""
     esz = 2 if inp["dtype"] == "bf16" else 4
     kv = sum(int(L) + inp["N"] for L in inp["seq_lens"]) * inp["Hkv"] * inp["D"] * esz * 2
     qo = 2 * inp["B"] * inp["N"] * inp["Hq"] * inp["D"] * esz
-    return kv + qo
+    new_rows = 2 * 2 * inp["B"] * inp["N"] * inp["Hkv"] * inp["D"] * esz if append else 0
+    return kv + qo + new_rows
+
+
+def tree_rows(inp):
+    """The tree nodes' K/V rows [B, N, Hkv, D] as the generator placed them in the cache
+    (slots L_b .. L_b + N - 1): the step's new K/V, appended by the attention call."""
+    B, N, bs = inp["B"], inp["N"], inp["block_size"]
+    t = inp["seq_lens"][:, None].astype(np.int64) + np.arange(N)[None, :]
+    blk = np.take_along_axis(inp["block_table"], t // bs, axis=1)
+    return (np.ascontiguousarray(inp["k_cache"][blk, t % bs]), np.ascontiguousarray(inp["v_cache"][blk, t % bs]))
 
 
 def attn_flops(inp):
@@ -364,7 +376,9 @@ def run_ours(args, rank, world, local_rank):
             t = t.view(dtype)
         return t.pin_memory()
 
-    H = dict(q=host(inp["q"], el), k_cache=host(inp["k_cache"], el), v_cache=host(inp["v_cache"], el),
+    k_new, v_new = tree_rows(inp)
+    H = dict(q=host(inp["q"], el), k_new=host(k_new, el), v_new=host(v_new, el),
+             k_cache=host(inp["k_cache"], el), v_cache=host(inp["v_cache"], el),
              block_table=host(inp["block_table"]), seq_lens=host(inp["seq_lens"]), parent=host(inp["parent"]),
              target_logits=host(inp["target_logits"]), draft_probs=host(inp["draft_probs"]),
              draft_tokens=host(inp["draft_tokens"]), u_accept=host(inp["u_accept"]), u_bonus=host(inp["u_bonus"]))
@@ -382,8 +396,10 @@ def run_ours(args, rank, world, local_rank):
     def step(ev=None):
         if ev is not None:
             ev[0].record(stream)
-        tsv.tree_verify_attn(Dv["q"], Dv["k_cache"], Dv["v_cache"], Dv["block_table"], Dv["seq_lens"],
-                             Dv["parent"], out, inp["scale"], workspace=ws if ws_bytes else None, seq_err=attn_err)
+        # the tree's K/V rows are written into the cache by the attention call itself
+        tsv.tree_verify_attn_append(Dv["q"], Dv["k_new"], Dv["v_new"], Dv["k_cache"], Dv["v_cache"],
+                                    Dv["block_table"], Dv["seq_lens"], Dv["parent"], out, inp["scale"],
+                                    workspace=ws if ws_bytes else None, seq_err=attn_err)
         if ev is not None:
             ev[1].record(stream)
         # the walk with the KV-cache rewrite of its accepted path in its tail
@@ -453,7 +469,7 @@ def run_ours(args, rank, world, local_rank):
         e["binding_frac"] = round(max(t_hbm, t_tc) / t, 4)
         return e
 
-    per_kernel = {"tree_verify_attn": kernel_entry(a_bytes, a_flops, mean_ms[0]),
+    per_kernel = {"tree_verify_attn_append": kernel_entry(a_bytes, a_flops, mean_ms[0]),
                   "tree_reject_sample_compact": kernel_entry(w_bytes, 0, mean_ms[1])}
     dom = max(per_kernel, key=lambda k: per_kernel[k]["avg_us"])
     d = per_kernel[dom]
@@ -494,8 +510,8 @@ def run_ours(args, rank, world, local_rank):
     e2e = {"value": whole_job_rate(tokens_per_step * K, e2e_s, world), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
            "d2h_bytes_per_step": int(d2h)}
 
-    # bf16: check, persistent attention and merge kernels; fp32: attention (+ merge when split)
-    attn_launches = 3 if inp["dtype"] == "bf16" else 1 + (1 if ws_bytes else 0)
+    # bf16: check (+ append), persistent attention and merge kernels; fp32: append, attention (+ merge when split)
+    attn_launches = 3 if inp["dtype"] == "bf16" else 2 + (1 if ws_bytes else 0)
     launches_per_step = attn_launches + 1  # + the walk with its fused rewrite
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,

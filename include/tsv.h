@@ -109,6 +109,30 @@ tsv_status tsv_tree_verify_attn(const void *q, const void *k_cache, const void *
                                 int32_t *seq_err, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * tsv_tree_verify_attn with the tree's own K/V appended in the same call (sglang
+ * report, "Tree-based Speculative Decoding (EAGLE) Implementation Summary": the KV
+ * cache is updated for the tree's tokens before they are verified; vLLM PR #2188,
+ * "Guide for reviewers": no host synchronisation inside the step).
+ *
+ * k_new, v_new [B, N, Hkv, D] (dtype as q) are the tree nodes' K/V rows; node j's row
+ * is written to logical slot seq_lens[b] + j of k_cache / v_cache (all kv heads), and
+ * the attention then reads it there, exactly as tsv_tree_verify_attn does once the
+ * caller has written the rows: same results, same workspace, same errors.  A sequence
+ * whose capacity or block ids fail the checks (TSV_DERR_CAPACITY / TSV_DERR_BLOCK)
+ * gets no rows written.  The rows are written by the sequence-check kernel, and the
+ * attention kernel waits for that kernel (programmatic dependent launch) before its
+ * first tile that reaches the tree keys, so the append adds no launch on the bf16
+ * path (fp32: one small kernel before the attention).  k_new / v_new must be 16-byte
+ * aligned and must not overlap the caches.
+ * ------------------------------------------------------------------------- */
+tsv_status tsv_tree_verify_attn_append(const void *q, const void *k_new, const void *v_new, void *k_cache,
+                                       void *v_cache, const int32_t *block_table,
+                                       const int32_t *seq_lens, const int32_t *parent, void *out, int B,
+                                       int N, int Hq, int Hkv, int D, int block_size, int max_blocks,
+                                       int num_blocks, float scale, tsv_dtype dtype, void *workspace,
+                                       size_t workspace_bytes, int32_t *seq_err, void *stream);
+
+/* ---------------------------------------------------------------------------
  * tsv_tree_verify_attn without a caller workspace (the pages have no counterpart
  * of this call; it is an interface convenience).
  *

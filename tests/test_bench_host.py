@@ -12,7 +12,9 @@ import workloads as W
 def test_algorithmic_bytes():
     inp = W.generate(W.CONFIGS[1].replace(B=2, V=64))
     # K and V of 2054 slots x 8 heads x 128 dims x 2 bytes, both sequences; Q in and O out
-    assert bench.attn_bytes(inp) == 2 * 2054 * 8 * 128 * 2 * 2 + 2 * 2 * 6 * 32 * 128 * 2
+    assert bench.attn_bytes(inp, append=False) == 2 * 2054 * 8 * 128 * 2 * 2 + 2 * 2 * 6 * 32 * 128 * 2
+    # the fused append also reads the tree's new K/V rows and writes them into the cache
+    assert bench.attn_bytes(inp) - bench.attn_bytes(inp, append=False) == 2 * 2 * 2 * 6 * 8 * 128 * 2
     an = np.array([[0, 1, 2, -1, -1, -1], [0, -1, -1, -1, -1, -1]])
     al = np.array([2, 0])
     # seq 0 visits 3 nodes; first children accepted at 0 and 1; node 2 rejects its child -> draft row read
@@ -63,3 +65,15 @@ def test_parity_summary_counts_identical_exempt_and_mismatched():
     p = bench.parity_summary(inp, g, o, rows, want, got)
     assert (p["identical"], p["exempt_near_ties"], p["mismatched"]) == (4, 1, 1)
     assert p["attn_max_abs_err"] == 0.01 and not p["ok"]
+
+
+def test_tree_rows_are_the_cache_slots_after_each_prefix():
+    inp = W.generate(W.CONFIGS[3].replace(B=3, Hq=4, Hkv=2, D=64, prefix=(5, 70), N=9, depth=4, V=32, seed=2))
+    kn, vn = bench.tree_rows(inp)
+    bs = inp["block_size"]
+    for b in range(3):
+        for j in range(9):
+            t = int(inp["seq_lens"][b]) + j
+            blk = inp["block_table"][b, t // bs]
+            assert np.array_equal(kn[b, j], inp["k_cache"][blk, t % bs])
+            assert np.array_equal(vn[b, j], inp["v_cache"][blk, t % bs])

@@ -57,6 +57,8 @@ def load():
     lib.tsv_attn_workspace_size.argtypes = [i32] * 8
     lib.tsv_tree_verify_attn.restype = i32
     lib.tsv_tree_verify_attn.argtypes = [P] * 7 + [i32] * 8 + [f32, i32, P, sz, P, P]
+    lib.tsv_tree_verify_attn_append.restype = i32
+    lib.tsv_tree_verify_attn_append.argtypes = [P] * 9 + [i32] * 8 + [f32, i32, P, sz, P, P]
     lib.tsv_tree_reject_sample.restype = i32
     lib.tsv_tree_reject_sample.argtypes = [P, P, P, P, P, P, f32, i32, i32, i32, P, P, P, P, P, P]
     lib.tsv_tree_verify_attn_noalloc.restype = i32
@@ -138,6 +140,20 @@ def tree_verify_attn(q, k_cache, v_cache, block_table, seq_lens, parent, out, sc
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens), _ptr(parent), _ptr(out),
         B, N, Hq, Hkv, D, bs, block_table.shape[1], num_blocks, float(scale), _dtype_code(q),
         _ptr(workspace), ws_bytes, _ptr(seq_err), _stream(stream)))
+
+
+def tree_verify_attn_append(q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, parent, out, scale: float,
+                            workspace=None, seq_err=None, stream=None):
+    """tree_verify_attn that first writes the tree's K/V rows (k_new / v_new
+    [B,N,Hkv,D]) into the cache at logical slots seq_lens[b] + j (see include/tsv.h)."""
+    _contig(q, k_new, v_new, k_cache, v_cache, block_table, seq_lens, parent, out, workspace, seq_err)
+    B, N, Hq, D = q.shape
+    num_blocks, bs, Hkv, _ = k_cache.shape
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().tsv_tree_verify_attn_append(
+        _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache), _ptr(block_table), _ptr(seq_lens),
+        _ptr(parent), _ptr(out), B, N, Hq, Hkv, D, bs, block_table.shape[1], num_blocks, float(scale),
+        _dtype_code(q), _ptr(workspace), ws_bytes, _ptr(seq_err), _stream(stream)))
 
 
 def tree_verify_attn_noalloc(q, k_cache, v_cache, block_table, seq_lens, parent, out, scale: float,

@@ -101,16 +101,22 @@ size_t tsv_attn_workspace_size(int B, int N, int Hq, int Hkv, int D, int block_s
     return plan_for(B, N, Hq, Hkv, D, block_size, max_blocks, dtype).ws_bytes;
 }
 
-tsv_status tsv_tree_verify_attn(const void* q, const void* k_cache, const void* v_cache,
-                                const int32_t* block_table, const int32_t* seq_lens, const int32_t* parent,
-                                void* out, int B, int N, int Hq, int Hkv, int D, int block_size, int max_blocks,
-                                int num_blocks, float scale, tsv_dtype dtype, void* workspace,
-                                size_t workspace_bytes, int32_t* seq_err, void* stream) {
+}  // extern "C"
+
+namespace {
+// The attention call, with the fused append of the tree's rows when k_new != nullptr.
+tsv_status verify_attn(const void* q, const void* k_new, const void* v_new, void* k_cache_w, void* v_cache_w,
+                       const void* k_cache, const void* v_cache, const int32_t* block_table, const int32_t* seq_lens,
+                       const int32_t* parent, void* out, int B, int N, int Hq, int Hkv, int D, int block_size,
+                       int max_blocks, int num_blocks, float scale, tsv_dtype dtype, void* workspace,
+                       size_t workspace_bytes, int32_t* seq_err, void* stream) {
     tsv_status st = check_attn_shapes(B, N, Hq, Hkv, D, block_size, max_blocks, num_blocks, dtype);
     if (st != TSV_OK) return st;
     if (B == 0) return TSV_OK;
     if (!q || !k_cache || !v_cache || !block_table || !seq_lens || !parent || !out || !seq_err)
         return fail(TSV_ERR_ARG, "null array argument");
+    if (k_new != nullptr && (!v_new || !aligned16(k_new) || !aligned16(v_new)))
+        return fail(TSV_ERR_ARG, "k_new and v_new must be non-null and 16-byte aligned");
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
         return fail(TSV_ERR_ARG, "q, caches and out must be 16-byte aligned");
     if (!(scale > 0.0f) || !isfinite(scale)) return fail(TSV_ERR_ARG, "scale must be positive and finite");
@@ -123,6 +129,10 @@ tsv_status tsv_tree_verify_attn(const void* q, const void* k_cache, const void* 
     a.q = q;
     a.k_cache = k_cache;
     a.v_cache = v_cache;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.k_cache_w = k_cache_w;
+    a.v_cache_w = v_cache_w;
     a.block_table = block_table;
     a.seq_lens = seq_lens;
     a.parent = parent;
@@ -162,6 +172,30 @@ tsv_status tsv_tree_verify_attn(const void* q, const void* k_cache, const void* 
     }
     if (e != cudaSuccess) return cuda_fail(e, "tree_verify_attn launch");
     return TSV_OK;
+}
+}  // namespace
+
+extern "C" {
+
+tsv_status tsv_tree_verify_attn(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_table, const int32_t* seq_lens, const int32_t* parent,
+                                void* out, int B, int N, int Hq, int Hkv, int D, int block_size, int max_blocks,
+                                int num_blocks, float scale, tsv_dtype dtype, void* workspace,
+                                size_t workspace_bytes, int32_t* seq_err, void* stream) {
+    return verify_attn(q, nullptr, nullptr, nullptr, nullptr, k_cache, v_cache, block_table, seq_lens, parent, out, B,
+                       N, Hq, Hkv, D, block_size, max_blocks, num_blocks, scale, dtype, workspace, workspace_bytes,
+                       seq_err, stream);
+}
+
+tsv_status tsv_tree_verify_attn_append(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                                       void* v_cache, const int32_t* block_table, const int32_t* seq_lens,
+                                       const int32_t* parent, void* out, int B, int N, int Hq, int Hkv, int D,
+                                       int block_size, int max_blocks, int num_blocks, float scale, tsv_dtype dtype,
+                                       void* workspace, size_t workspace_bytes, int32_t* seq_err, void* stream) {
+    if (B > 0 && (!k_new || !v_new)) return fail(TSV_ERR_ARG, "null k_new / v_new");
+    return verify_attn(q, k_new, v_new, k_cache, v_cache, k_cache, v_cache, block_table, seq_lens, parent, out, B, N,
+                       Hq, Hkv, D, block_size, max_blocks, num_blocks, scale, dtype, workspace, workspace_bytes, seq_err,
+                       stream);
 }
 
 }  // extern "C"

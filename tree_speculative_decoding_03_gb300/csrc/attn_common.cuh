@@ -93,6 +93,12 @@ struct AttnArgs {
     const void* q;
     const void* k_cache;
     const void* v_cache;
+    // fused append: the tree's K/V rows [B, N, Hkv, D] written into the caches (at
+    // logical slots L_b .. L_b + N - 1) before they are read; k_new == nullptr: none
+    const void* k_new;
+    const void* v_new;
+    void* k_cache_w;
+    void* v_cache_w;
     const int32_t* block_table;
     const int32_t* seq_lens;
     const int32_t* parent;

@@ -226,8 +226,25 @@ static cudaError_t launch_simt_inst(const AttnArgs& a, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// Fused append on the FMA path: one CTA per sequence writes the tree's rows where the
+// capacity and block ids allow it (the attention kernel after it in the stream checks
+// and reports the sequence).
+__global__ void __launch_bounds__(128) attn_append_kernel(const AttnArgs a) {
+    __shared__ int s_flag;
+    const int b = blockIdx.x;
+    const int L = a.seq_lens[b];
+    const int32_t* bt = a.block_table + (long long)b * a.max_blocks;
+    if (block_cache_errors(bt, L, a.N, 1 << a.bs_log2, a.max_blocks, a.num_blocks, &s_flag)) return;
+    append_tree_rows(a.k_new, a.v_new, a.k_cache_w, a.v_cache_w, bt, b, L, a.N, a.Hkv * a.D * 4, a.bs_log2);
+}
+
 // fp32 inputs only: bf16 runs on the tensor-core kernel (attn_tc.cu)
 cudaError_t launch_attn_simt_f32(const AttnArgs& a, cudaStream_t stream) {
+    if (a.k_new != nullptr) {
+        attn_append_kernel<<<a.B, 128, 0, stream>>>(a);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     return a.D == 64 ? launch_simt_inst<64>(a, stream) : launch_simt_inst<128>(a, stream);
 }
 

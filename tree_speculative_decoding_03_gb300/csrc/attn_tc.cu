@@ -418,8 +418,9 @@ __device__ __forceinline__ void find_start(const AttnArgs& a, int lane_c, int* s
 }
 
 // One CTA per sequence, alongside the attention kernel: the checks behind seq_err[b]
-// (capacity first; a parent array that is not a tree; a block id outside the cache).
-__global__ void __launch_bounds__(128) attn_tc_check_kernel(const AttnArgs a) {
+// (capacity first; a parent array that is not a tree; a block id outside the cache),
+// and with the fused append the tree's new K/V rows (256 threads then, 128 without).
+__global__ void __launch_bounds__(256) attn_tc_check_kernel(const AttnArgs a) {
     __shared__ int s_flag;
     // the inputs may come from the previous kernel in the stream: wait for it before the
     // attention kernel (which reads them too) is allowed to start
@@ -433,6 +434,12 @@ __global__ void __launch_bounds__(128) attn_tc_check_kernel(const AttnArgs a) {
     if (cap_ok)
         e |= block_cache_errors(a.block_table + (long long)b * a.max_blocks, L, N, 1 << a.bs_log2, a.max_blocks,
                                 a.num_blocks, &s_flag);
+    // fused append: the tree's rows go into the cache here, where the block ids have just
+    // been checked; the attention kernel waits for this kernel before its first tile
+    // that reaches the tree keys
+    if (a.k_new != nullptr && cap_ok && !(e & TSV_DERR_BLOCK))
+        append_tree_rows(a.k_new, a.v_new, a.k_cache_w, a.v_cache_w, a.block_table + (long long)b * a.max_blocks, b, L,
+                         N, a.Hkv * a.D * 2, a.bs_log2);
     if (threadIdx.x == 0) a.seq_err[b] = e;
 }
 
@@ -504,10 +511,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         int blk = (count > 0 && lane < 16) ? s_blk0[lane] : 0;  // looked up during set-up
         const uint64_t kv_policy = l2_evict_first_policy();  // every K/V row is read once
         int seg = 0;
+        bool appended = a.k_new == nullptr;  // the tree rows this kernel reads are in the cache
         for (int jt = 0; jt < count && !my_err; ++jt) {
             if (jt > 0 && it.t == 0) ++seg;
             const bool first = (jt == 0) || (it.t == 0);
             const int t0 = it.t * kTileKeys;
+            if (!appended && t0 + kTileKeys > it.L) {
+                // a tile with tree keys: the check kernel before this one in the stream has
+                // written them (its memory is visible once it has completed); the copies
+                // then read them through the async proxy
+                pdl_wait();
+                asm volatile("fence.proxy.async.global;" ::: "memory");
+                appended = true;
+            }
             const int nblk = (min(t0 + kTileKeys, it.L + N) - t0 + bs - 1) >> a.bs_log2;
             const int g = it.g;
             const int blk_cur = blk;
@@ -1148,7 +1164,8 @@ cudaError_t launch_tc_inst(const AttnArgs& a, cudaStream_t stream) {
     }
     const CUtensorMap& mk = mc.mk;
     const CUtensorMap& mv = mc.mv;
-    cudaError_t e = launch_pdl(attn_tc_check_kernel, dim3(static_cast<unsigned>(a.B)), dim3(128), 0, stream, 1u, a);
+    cudaError_t e = launch_pdl(attn_tc_check_kernel, dim3(static_cast<unsigned>(a.B)), dim3(a.k_new ? 256 : 128), 0,
+                               stream, 1u, a);
     if (e != cudaSuccess) return e;
     const int nm_max = a.R > 128 ? 2 : 1;
     const TcLayout lay = tc_layout<D>(nm_max);

@@ -100,6 +100,42 @@ __device__ __forceinline__ void build_ancestor_masks(const int32_t* par, int N, 
 
 __device__ __forceinline__ bool anc_has(const uint32_t* m, int j) { return (m[j >> 5] >> (j & 31)) & 1u; }
 
+// Writes the tree's new K/V rows of sequence b (k_new / v_new [B, N, Hkv, D], one
+// row = row_bytes contiguous bytes: all kv heads of a node) into the paged caches at
+// logical slots L .. L + N - 1, in 16-byte vectors (row_bytes is a multiple of 16 and
+// every base is 16-byte aligned).  The block ids covering [0, L + N) must have been
+// checked.  Cooperative over the calling block.
+__device__ __forceinline__ void append_tree_rows(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                                                 const int32_t* bt_row, int b, int L, int N, int row_bytes,
+                                                 int bs_log2) {
+    const int vecs = row_bytes >> 4;  // 16-byte vectors per row
+    const long long src0 = (long long)b * N * vecs;
+    const int total = 2 * N * vecs;     // K rows first, then V rows
+    constexpr int U = 4;                // vectors in flight per thread
+    for (int base = 0; base < total; base += U * (int)blockDim.x) {
+        uint4 val[U];
+        long long dst[U];
+        int kvs[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int idx = base + u * (int)blockDim.x + (int)threadIdx.x;
+            kvs[u] = -1;
+            if (idx < total) {
+                const int kv = idx >= N * vecs;
+                const int r = kv ? idx - N * vecs : idx;
+                const int j = r / vecs, c = r - j * vecs;
+                const int t = L + j;
+                dst[u] = ((long long)bt_row[t >> bs_log2] * (1 << bs_log2) + (t & ((1 << bs_log2) - 1))) * vecs + c;
+                val[u] = __ldg(static_cast<const uint4*>(kv ? v_new : k_new) + src0 + (long long)j * vecs + c);
+                kvs[u] = kv;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (kvs[u] >= 0) static_cast<uint4*>(kvs[u] ? v_cache : k_cache)[dst[u]] = val[u];
+    }
+}
+
 // Physical row of logical slot t (block ids already validated by the caller).
 __device__ __forceinline__ long long phys_row(const int32_t* bt_row, int t, int bs_log2) {
     return (long long)bt_row[t >> bs_log2] * (1 << bs_log2) + (t & ((1 << bs_log2) - 1));
