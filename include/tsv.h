@@ -67,8 +67,10 @@ enum {
     TSV_DERR_CAPACITY = 4,  /* L_b < 0 or L_b + N > max_blocks * block_size */
     TSV_DERR_TOKEN = 8,     /* a tried draft token is outside [0, V) */
     TSV_DERR_NONFINITE = 16, /* a visited logits row, or a draft row that is read, is not finite */
-    TSV_DERR_TIMEOUT = 32    /* internal: a bounded device-side wait gave up; outputs of the
+    TSV_DERR_TIMEOUT = 32,   /* internal: a bounded device-side wait gave up; outputs of the
                                 sequence are not valid (never expected; reported, not trapped) */
+    TSV_DERR_INTERNAL = 64   /* checked builds only (-DTSV_CHECKED, a test build): a device-side
+                                index check failed and the access was skipped -- a library bug */
 };
 
 /* Message for the calling thread's most recent failed call ("" if none). */

@@ -20,9 +20,11 @@ TSV_OK, TSV_ERR_ARG, TSV_ERR_UNSUPPORTED, TSV_ERR_CUDA = 0, 1, 2, 3
 TSV_BF16, TSV_F32 = 0, 1
 # device-side data error bits in seq_err (include/tsv.h)
 TSV_DERR_PARENT, TSV_DERR_BLOCK, TSV_DERR_CAPACITY, TSV_DERR_TOKEN, TSV_DERR_NONFINITE, TSV_DERR_TIMEOUT = 1, 2, 4, 8, 16, 32
+TSV_DERR_INTERNAL = 64  # checked test build only
 DERR_PARENT, DERR_BLOCK, DERR_CAPACITY, DERR_TOKEN, DERR_NONFINITE = 1, 2, 4, 8, 16
 
-_lib = None
+_libs = {}           # loaded libraries by build variant (None = the product build)
+_variant = None      # the variant load() returns by default (tests switch it)
 
 
 class TsvError(RuntimeError):
@@ -31,22 +33,31 @@ class TsvError(RuntimeError):
         self.status = status
 
 
-def lib_path() -> str:
-    from .builder import LIB
-    return LIB
+def lib_path(variant=None) -> str:
+    from .builder import lib_path as _p
+    return _p(variant)
 
 
-def build(verbose: bool = False) -> str:
+def build(verbose: bool = False, variant=None) -> str:
+    """Builds the library: the product build, or a test build ("checked": device-side
+    index checks; "hooks": short bounded waits and a stall switch)."""
     from .builder import build_library
-    return build_library(verbose=verbose)
+    return build_library(verbose=verbose, variant=variant)
 
 
-def load():
+def use_variant(variant=None):
+    """Makes load() -- and so every call of this module -- use a test build (None: the
+    product build).  For tests only."""
+    global _variant
+    _variant = variant
+
+
+def load(variant=None):
     """Loads the in-tree libtsv.so (raises if it has not been built)."""
-    global _lib
-    if _lib is not None:
-        return _lib
-    path = lib_path()
+    v = _variant if variant is None else variant
+    if v in _libs:
+        return _libs[v]
+    path = lib_path(v)
     if not os.path.exists(path):
         raise RuntimeError(f"libtsv.so not built at {path}; run build() first")
     lib = ctypes.CDLL(path)
@@ -84,7 +95,10 @@ def load():
     lib.tsv_sequoia_plan.argtypes = [P, i32, i32, i32, P, f64, P, P, P]
     lib.tsv_sequoia_accept_counts.restype = i32
     lib.tsv_sequoia_accept_counts.argtypes = [P, P, P, i32, i32, i32, P, P]
-    _lib = lib
+    if hasattr(lib, "tsv_test_set_stall"):  # the "hooks" test build only
+        lib.tsv_test_set_stall.restype = i32
+        lib.tsv_test_set_stall.argtypes = [i32]
+    _libs[v] = lib
     return lib
 
 

@@ -33,20 +33,35 @@ def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+# Test builds of the same sources: "checked" adds device-side index checks
+# (-DTSV_CHECKED), "hooks" shortens the bounded waits and adds a stall switch
+# (-DTSV_TEST_HOOKS).  Each is built into its own folder; the product library is the
+# default (no variant).
+VARIANT_FLAGS = {"checked": ["-DTSV_CHECKED"], "hooks": ["-DTSV_TEST_HOOKS"]}
+
+
+def lib_path(variant=None) -> str:
+    return LIB if variant is None else os.path.join(OUT_DIR, variant, "libtsv.so")
+
+
+def up_to_date(variant=None) -> bool:
+    lib = lib_path(variant)
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build_library(verbose: bool = False, extra_flags=()) -> str:
-    if up_to_date() and not extra_flags:
-        return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build_library(verbose: bool = False, extra_flags=(), variant=None) -> str:
+    lib = lib_path(variant)
+    extra_flags = list(extra_flags) + VARIANT_FLAGS.get(variant, [])
+    if up_to_date(variant) and not (extra_flags and variant is None):
+        return lib
+    out_dir = os.path.dirname(lib)
+    os.makedirs(out_dir, exist_ok=True)
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
+        obj = os.path.join(out_dir, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [NVCC, *ARCH, *FLAGS, *extra_flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -57,13 +72,13 @@ def build_library(verbose: bool = False, extra_flags=()) -> str:
 
     with ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [NVCC, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

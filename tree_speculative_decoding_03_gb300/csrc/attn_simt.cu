@@ -235,7 +235,9 @@ __global__ void __launch_bounds__(128) attn_append_kernel(const AttnArgs a) {
     const int L = a.seq_lens[b];
     const int32_t* bt = a.block_table + (long long)b * a.max_blocks;
     if (block_cache_errors(bt, L, a.N, 1 << a.bs_log2, a.max_blocks, a.num_blocks, &s_flag)) return;
-    append_tree_rows(a.k_new, a.v_new, a.k_cache_w, a.v_cache_w, bt, b, L, a.N, a.Hkv * a.D * 4, a.bs_log2);
+    append_tree_rows(a.k_new, a.v_new, a.k_cache_w, a.v_cache_w, bt, b, L, a.N, a.Hkv * a.D * 4, a.bs_log2,
+                     ((long long)a.num_blocks << a.bs_log2) * a.Hkv * a.D * 4 / 16,
+                     (long long)a.B * a.N * a.Hkv * a.D * 4 / 16, a.seq_err + b);
 }
 
 // fp32 inputs only: bf16 runs on the tensor-core kernel (attn_tc.cu)

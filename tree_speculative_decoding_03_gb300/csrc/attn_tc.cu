@@ -52,7 +52,14 @@ constexpr int kThreads = 384;
 constexpr int kTileKeys = 128;
 constexpr uint32_t kHalfBytes = 128 * 128;   // 128 rows x 64 bf16 (one 128B-swizzled half)
 constexpr int kMaxSlots = 12;
+#ifdef TSV_TEST_HOOKS
+// test build only: waits give up after 1 ms, and one wait can be pointed at a barrier
+// that nothing completes (tsv_test_set_stall), so a test can drive the timeout path
+constexpr unsigned long long kWaitLimitNs = 1000000ull;
+__device__ int g_test_stall = 0;
+#else
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;
+#endif
 // A CTA with few tiles sends its first K/V tile out alone and waits for the K half before
 // filling the rest of the ring: at start-up every such CTA's first tile then sits at the
 // front of the DRAM queue instead of behind every CTA's whole ring (measured: chain5
@@ -304,7 +311,8 @@ struct Bars {
     static constexpr int kO = kP + 2;         // [2]
     static constexpr int kQ = kO + 2;         // one phase per segment
     static constexpr int kDone = kQ + 1;
-    static constexpr int kCount = kDone + 1;
+    static constexpr int kStall = kDone + 1;  // never completed (test build: the stalled wait)
+    static constexpr int kCount = kStall + 1;
 };
 
 // misc region (512 bytes): parents of the segment's sequence (int8, two buffers by
@@ -437,10 +445,12 @@ __global__ void __launch_bounds__(256) attn_tc_check_kernel(const AttnArgs a) {
     // fused append: the tree's rows go into the cache here, where the block ids have just
     // been checked; the attention kernel waits for this kernel before its first tile
     // that reaches the tree keys
+    if (threadIdx.x == 0) a.seq_err[b] = e;
+    __syncthreads();  // the checked build's index checks may add a bit to it below
     if (a.k_new != nullptr && cap_ok && !(e & TSV_DERR_BLOCK))
         append_tree_rows(a.k_new, a.v_new, a.k_cache_w, a.v_cache_w, a.block_table + (long long)b * a.max_blocks, b, L,
-                         N, a.Hkv * a.D * 2, a.bs_log2);
-    if (threadIdx.x == 0) a.seq_err[b] = e;
+                         N, a.Hkv * a.D * 2, a.bs_log2, ((long long)a.num_blocks << a.bs_log2) * a.Hkv * a.D * 2 / 16,
+                         (long long)a.B * N * a.Hkv * a.D * 2 / 16, a.seq_err + b);
 }
 
 template <int D>
@@ -484,6 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bar(Bars::kQ), 128 * nm);
         mbar_init(bar(Bars::kDone), 1);
+        mbar_init(bar(Bars::kStall), 1);
         *s_abort = 0;
         fence_barrier_init();
     }
@@ -512,6 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t kv_policy = l2_evict_first_policy();  // every K/V row is read once
         int seg = 0;
         bool appended = a.k_new == nullptr;  // the tree rows this kernel reads are in the cache
+        int issued = 0;                      // fills issued so far
         for (int jt = 0; jt < count && !my_err; ++jt) {
             if (jt > 0 && it.t == 0) ++seg;
             const bool first = (jt == 0) || (it.t == 0);
@@ -555,14 +567,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_3d(dst + hh * kHalfBytes + lane * bs * 128, map, bar(Bars::kFull + slot), hh * 64, g,
                                     blk_cur * bs, kv_policy);
                 }
+                issued = f + 1;
             }
             if (jt == 0 && count > 1 && count <= kFirstTileAloneMaxTiles && !my_err &&
                 !__all_sync(0xffffffffu, mbar_wait(bar(Bars::kFull + 0), 0, s_abort)))
                 my_err = 1;
         }
-        // never leave with copies in flight: wait for the latest fill of every slot
+        // never leave with copies in flight: wait for the latest issued fill of every slot
+        // (after an abort, fills that were never issued are not waited for)
         if (lane == 0) {
-            for (int f = max(0, 2 * count - nslots); f < 2 * count; ++f) {
+            for (int f = max(0, issued - nslots); f < issued; ++f) {
                 volatile int never = 0;
                 if (!mbar_wait(bar(Bars::kFull + f % nslots), (f / nslots) & 1, &never)) my_err = 1;
             }
@@ -731,11 +745,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // are formed here instead of being kept in registers across the tile loop
             const uint32_t r7 = opaque_u32(static_cast<uint32_t>(tw & 7));
             const uint32_t dst = smem_u32(smem + lay.q0 + wg * (128u * D * 2u)) + (tw >> 3) * 1024u + r7 * 128u;
-            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
-                                                              (((long long)bq * N + n) * a.Hq + gq * a.G + hj) * D);
+            const long long qrow = (((long long)bq * N + n) * a.Hq + gq * a.G + hj) * D;
+            const bool take = valid && TSV_IN_BOUNDS(qrow + D - 1, (long long)a.B * N * a.Hq * D, a.seq_err + bq);
+            const uint4* src = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + (take ? qrow : 0));
 #pragma unroll
             for (int qq = 0; qq < D / 8; ++qq)
-                cp_async16(dst + (qq >> 3) * kHalfBytes + (((qq & 7) ^ r7) << 4), src + qq, valid);
+                cp_async16(dst + (qq >> 3) * kHalfBytes + (((qq & 7) ^ r7) << 4), src + qq, take);
         };
         auto finish_q = [&]() {
             cp_async_wait_all();
@@ -763,7 +778,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // segment's last tile, once that tile's S product (the last reader of Q) is done
             const bool more = jt + ntl < count;
             err_b = b;
-            if (t_first == 0 && stid == 0) {
+            if (t_first == 0 && stid == 0 &&
+                TSV_IN_BOUNDS(((long long)b * a.Hkv + g) * nrg + rg, (long long)a.B * a.Hkv * nrg, a.seq_err + b)) {
                 // this lane holds the unit's first piece: record where its pieces are
                 int* ui = a.unit_info + (((long long)b * a.Hkv + g) * nrg + rg) * kUnitInfoInts;
                 ui[0] = lane_c;
@@ -800,7 +816,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int sb = nm == 2 ? wg : (jt & 1);
                 const uint32_t sphase = nm == 2 ? (jt & 1) : ((jt >> 1) & 1);
                 const uint32_t tS = tS0 + sb * 128;
+#ifdef TSV_TEST_HOOKS
+                // the stalled wait: warpgroup 0's first S never arrives, the wait gives up
+                const bool stall = g_test_stall != 0 && jt == 0 && wg == 0;
+                ok = __all_sync(0xffffffffu, mbar_wait(bar(stall ? Bars::kStall : Bars::kS + sb), sphase, s_abort));
+#else
                 ok = __all_sync(0xffffffffu, mbar_wait(bar(Bars::kS + sb), sphase, s_abort));
+#endif
                 if (!ok) {
                     *s_abort = 1;
                     continue;
@@ -934,12 +956,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const float inv = l_run > 0.0f ? 1.0f / l_run : 0.0f;  // a piece may see no key of a row
                 const long long orow = (((long long)b * N + n) * a.Hq + g * a.G + hj) * D;
                 const long long prow = ((long long)blockIdx.x * 2 + side) * a.rows_item + wg * 128 + rl;
+                const bool in_bounds =
+                    !valid || (whole ? TSV_IN_BOUNDS(orow + D - 1, (long long)a.B * N * a.Hq * D, a.seq_err + b)
+                                     : TSV_IN_BOUNDS(prow, 2LL * gridDim.x * a.rows_item, a.seq_err + b));
 #pragma unroll 1
                 for (int q4 = 0; q4 < D / 32; ++q4) {
                     uint32_t ov[32];
                     tmem_ld32(tO + q4 * 32, ov);
                     tmem_wait_ld();
-                    if (valid) {
+                    if (valid && in_bounds) {
                         if (whole) {
                             uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(a.out) + orow + q4 * 32);
 #pragma unroll
@@ -964,7 +989,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                     }
                 }
-                if (valid && !whole) {
+                if (valid && !whole && in_bounds) {
                     a.part_m[prow] = m_run;
                     a.part_l[prow] = l_run;
                 }
@@ -1037,7 +1062,9 @@ __global__ void __launch_bounds__(256) attn_tc_merge_kernel(const AttnArgs a) {
         for (int k = 0; k < P; ++k) {
             lk[k] = 0.0f;
             mk[k] = -INFINITY;
-            if (c_first + k <= c_last) {
+            if (c_first + k <= c_last &&
+                TSV_IN_BOUNDS(((long long)((c_first + k) * nrg + rg) * 2 + (k == 0 ? sd0 : 0)) * a.rows_item + rr,
+                              2LL * a.lanes * nrg * a.rows_item, a.seq_err + b)) {
                 const long long pr = ((long long)((c_first + k) * nrg + rg) * 2 + (k == 0 ? sd0 : 0)) * a.rows_item + rr;
                 lk[k] = __ldg(a.part_l + pr);
                 mk[k] = __ldg(a.part_m + pr);
@@ -1192,6 +1219,13 @@ cudaError_t launch_tc_inst(const AttnArgs& a, cudaStream_t stream) {
 }  // namespace
 
 bool attn_tc_supported(int D) { return D == 64 || D == 128; }
+
+#ifdef TSV_TEST_HOOKS
+// test build only: 1 = the next attention calls stall one wait until it times out
+extern "C" int tsv_test_set_stall(int mode) {
+    return (int)cudaMemcpyToSymbol(g_test_stall, &mode, sizeof(int));
+}
+#endif
 int attn_tc_rows_per_cta() { return 256; }
 
 cudaError_t launch_attn_tc(const AttnArgs& a, cudaStream_t stream) {

@@ -12,6 +12,21 @@ namespace tsv {
 
 constexpr int kMaxNodes = 128;  // tree nodes per sequence, root included
 
+// Checked build (-DTSV_CHECKED, a test build): a global access through a computed
+// index is made only if the index lies inside its buffer; otherwise TSV_DERR_INTERNAL
+// is set in the given error word and the access is skipped.  The product build
+// compiles the checks away (the condition is not evaluated).
+__device__ __forceinline__ bool checked_in_bounds(long long i, long long n, int32_t* err) {
+    if (i >= 0 && i < n) return true;
+    if (err != nullptr) atomicOr(err, TSV_DERR_INTERNAL);
+    return false;
+}
+#ifdef TSV_CHECKED
+#define TSV_IN_BOUNDS(idx, extent, errp) (::tsv::checked_in_bounds((long long)(idx), (long long)(extent), (errp)))
+#else
+#define TSV_IN_BOUNDS(idx, extent, errp) true
+#endif
+
 // Programmatic dependent launch: every kernel of the library lets the next kernel in the
 // stream start launching early (pdl_launch_dependents) and waits for the previous one to
 // complete, with its writes visible, before reading anything (pdl_wait).  Without the
@@ -104,10 +119,12 @@ __device__ __forceinline__ bool anc_has(const uint32_t* m, int j) { return (m[j 
 // row = row_bytes contiguous bytes: all kv heads of a node) into the paged caches at
 // logical slots L .. L + N - 1, in 16-byte vectors (row_bytes is a multiple of 16 and
 // every base is 16-byte aligned).  The block ids covering [0, L + N) must have been
-// checked.  Cooperative over the calling block.
+// checked.  Cooperative over the calling block.  cache_vecs / new_vecs: 16-byte vectors
+// in a cache / in k_new (the checked build's bounds); err: the sequence's error word.
 __device__ __forceinline__ void append_tree_rows(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
                                                  const int32_t* bt_row, int b, int L, int N, int row_bytes,
-                                                 int bs_log2) {
+                                                 int bs_log2, long long cache_vecs, long long new_vecs,
+                                                 int32_t* err) {
     const int vecs = row_bytes >> 4;  // 16-byte vectors per row
     const long long src0 = (long long)b * N * vecs;
     const int total = 2 * N * vecs;     // K rows first, then V rows
@@ -126,6 +143,8 @@ __device__ __forceinline__ void append_tree_rows(const void* k_new, const void* 
                 const int j = r / vecs, c = r - j * vecs;
                 const int t = L + j;
                 dst[u] = ((long long)bt_row[t >> bs_log2] * (1 << bs_log2) + (t & ((1 << bs_log2) - 1))) * vecs + c;
+                if (!TSV_IN_BOUNDS(dst[u], cache_vecs, err) || !TSV_IN_BOUNDS(src0 + (long long)j * vecs + c, new_vecs, err))
+                    continue;
                 val[u] = __ldg(static_cast<const uint4*>(kv ? v_new : k_new) + src0 + (long long)j * vecs + c);
                 kvs[u] = kv;
             }

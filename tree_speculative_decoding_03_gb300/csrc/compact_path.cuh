@@ -65,6 +65,15 @@ __device__ __forceinline__ int compact_path(uint8_t* k_cache, uint8_t* v_cache, 
     const int nvec = row_bytes >> 4;  // vectors per row and cache
     const long long total = (long long)A * 2 * nvec;
     const int pass = kCompactVecs * (int)blockDim.x;
+    const long long cache_rows = (long long)num_blocks << bs_log2;
+#ifdef TSV_CHECKED
+    // checked build: a row index outside the cache skips the access and is reported
+    if (threadIdx.x == 0) *s_flag = 0;
+    __syncthreads();
+    int* const bad = s_flag;
+#else
+    int* const bad = nullptr;
+#endif
     for (long long base = 0; base < total; base += pass) {
         uint4 st[kCompactVecs];
 #pragma unroll
@@ -72,9 +81,10 @@ __device__ __forceinline__ int compact_path(uint8_t* k_cache, uint8_t* v_cache, 
             const long long i = base + threadIdx.x + u * (long long)blockDim.x;
             if (i < total) {
                 const int j = 1 + static_cast<int>(i / (2 * nvec)), w = static_cast<int>(i % (2 * nvec));
-                const long long src = phys_row(bt, L + s_path[j], bs_log2) * row_bytes;
+                const long long srow = phys_row(bt, L + s_path[j], bs_log2);
+                if (!TSV_IN_BOUNDS(srow, cache_rows, bad)) continue;
                 const uint8_t* cache = w < nvec ? k_cache : v_cache;
-                st[u] = reinterpret_cast<const uint4*>(cache + src)[w < nvec ? w : w - nvec];
+                st[u] = reinterpret_cast<const uint4*>(cache + srow * row_bytes)[w < nvec ? w : w - nvec];
             }
         }
         __syncthreads();
@@ -83,16 +93,22 @@ __device__ __forceinline__ int compact_path(uint8_t* k_cache, uint8_t* v_cache, 
             const long long i = base + threadIdx.x + u * (long long)blockDim.x;
             if (i < total) {
                 const int j = 1 + static_cast<int>(i / (2 * nvec)), w = static_cast<int>(i % (2 * nvec));
-                if (s_path[j] != j) {
-                    const long long dst = phys_row(bt, L + j, bs_log2) * row_bytes;
+                const long long drow = phys_row(bt, L + j, bs_log2);
+                if (s_path[j] != j && TSV_IN_BOUNDS(drow, cache_rows, bad) &&
+                    TSV_IN_BOUNDS(phys_row(bt, L + s_path[j], bs_log2), cache_rows, bad)) {
                     uint8_t* cache = w < nvec ? k_cache : v_cache;
-                    reinterpret_cast<uint4*>(cache + dst)[w < nvec ? w : w - nvec] = st[u];
+                    reinterpret_cast<uint4*>(cache + drow * row_bytes)[w < nvec ? w : w - nvec] = st[u];
                 }
             }
         }
         __syncthreads();
     }
+#ifdef TSV_CHECKED
+    return *bad ? TSV_DERR_INTERNAL : 0;
+#else
+    (void)bad;
     return 0;
+#endif
 }
 
 }  // namespace tsv

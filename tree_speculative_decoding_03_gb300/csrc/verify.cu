@@ -482,6 +482,10 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
     int amax = 0;
 
     while (!err) {
+        if (!TSV_IN_BOUNDS(node, N, a.seq_err + b)) {
+            err = TSV_DERR_INTERNAL;
+            break;
+        }
         const TL* lrow = static_cast<const TL*>(a.logits) + ((long long)b * N + node) * V;
         const float* qrow = greedy ? nullptr : a.probs + ((long long)b * N + node) * V;
         // children of `node`, in index order (warp 0, by ballot)
@@ -938,7 +942,8 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
     if (rank == 0) {
         for (int j = tid; j < N; j += blockDim.x) {
             a.accepted_nodes[rowoff + j] = j < plen ? s_path[j] : -1;
-            a.out_tokens[rowoff + j] = (j + 1 < plen) ? s_tok[s_path[j + 1]] : -1;
+            a.out_tokens[rowoff + j] =
+                (j + 1 < plen && TSV_IN_BOUNDS(s_path[j + 1], N, a.seq_err + b)) ? s_tok[s_path[j + 1]] : -1;
         }
         if (tid == 0) {
             a.accept_len[b] = plen - 1;
@@ -1120,6 +1125,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                 }
                 if (e_sel < 0) e_sel = e_last;
                 const int tok = v0 + (kseg * (int)blockDim.x + tid) * 4 + e_sel;
+                (void)TSV_IN_BOUNDS(tok, V, a.seq_err + b);  // a drawn token outside the vocabulary
                 a.bonus_token[b] = tok;
                 a.out_tokens[rowoff + plen - 1] = tok;
             }
