@@ -349,8 +349,15 @@ def parity_summary(inp, g, o, rows, attn_want, attn_got):
 
 # ----------------------------------------------------------------------------- our arm
 
-def run_ours(args, rank, world, local_rank):
+def _workload(args):
     w = W.CONFIGS[args.config]
+    if args.batch:  # a reduced batch of the same recipe (profiling captures that must stay small)
+        w = w.replace(B=args.batch, name=f"{w.name}_B{args.batch}")
+    return w
+
+
+def run_ours(args, rank, world, local_rank):
+    w = _workload(args)
     T = w.T if args.temperature is None else args.temperature
     inp = W.generate(w, temperature=T, seed=w.seed + 7919 * rank)
     # the CPU leg's oracle processes are forked before this process touches CUDA
@@ -545,7 +552,7 @@ def run_reference(args, rank, world):
     sample of the workload that cpu_baseline times (one sequence per process)."""
     if rank != 0:
         return
-    w = W.CONFIGS[args.config]
+    w = _workload(args)
     T = w.T if args.temperature is None else args.temperature
     inp = W.generate(w, temperature=T)
     budget = ORACLE_NODE_FLOP_BUDGET * 25 / max(1, args.steps + args.warmup) / 2  # whole run: a few minutes
@@ -575,6 +582,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=4, help="workload index (0..4); default 4, the serving mix")
     ap.add_argument("--temperature", type=float, default=None)
+    ap.add_argument("--batch", type=int, default=0, help="use the first B sequences' recipe with this batch size "
+                    "(reduced workloads for profiling captures; 0 = the workload's own)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parity", action="store_true", help="skip the oracle comparison of the timed call")
     args = ap.parse_args()
