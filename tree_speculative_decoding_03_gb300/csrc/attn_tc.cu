@@ -644,24 +644,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 for (int jt = 0; jt < count && ok; ++jt) {
                     const int fV = 2 * jt + 1, fK = 2 * jt + 2;
-                    ok = mbar_wait(bar(Bars::kFull + fV % nslots), (fV / nslots) & 1, s_abort);
-                    tc_fence_after();
+                    const int sV = fV % nslots, sK = fK % nslots;
+                    const bool nxt = jt + 1 < count;
+                    // everything this tile's products read besides P is waited for first, so each
+                    // M tile's PV and next S go to the tensor pipe back to back
+                    ok = mbar_wait(bar(Bars::kFull + sV), (fV / nslots) & 1, s_abort);
                     bool fnext = false;
+                    if (ok && nxt) ok = wait_K(jt + 1, &fnext);
+                    tc_fence_after();
                     for (int m = 0; m < nm && ok; ++m) {
                         ok = mbar_wait(bar(Bars::kP + m), jt & 1, s_abort);
                         if (!ok) break;
                         tc_fence_after();
-                        issue_PV(m, m, fV % nslots, !fcur);
+                        issue_PV(m, m, sV, !fcur);
+                        if (nxt) issue_S(m, m, sK);
                         mma_commit(bar(Bars::kO + m));
-                        if (m == nm - 1) mma_commit(bar(Bars::kEmpty + fV % nslots));  // V_jt's last reader issued
-                        if (jt + 1 < count) {
-                            if (m == 0) {
-                                ok = wait_K(jt + 1, &fnext);
-                                if (!ok) break;
-                            }
-                            issue_S(m, m, fK % nslots);
-                            mma_commit(bar(Bars::kS + m));
-                        }
+                        if (nxt) mma_commit(bar(Bars::kS + m));
+                        if (m == nm - 1) mma_commit(bar(Bars::kEmpty + sV));  // V_jt's last reader issued
                     }
                     if (!ok) break;
                     if (jt + 1 < count) mma_commit(bar(Bars::kEmpty + fK % nslots));
@@ -871,8 +870,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                fmaxf(mxa[6], mxa[7]));
                     const float mx = mx_raw * sl2;  // scale > 0: max commutes with it
                     // within a segment, the PV product of the previous tile must be done
-                    // before O is rescaled (a segment's first PV overwrites O)
-                    if (i > 0) {
+                    // before O is rescaled (a segment's first PV overwrites O).  With two M
+                    // tiles that is implied by the S just waited for: its issuer committed it
+                    // after that PV (a commit covers every earlier product of the issuing
+                    // thread).  With one, S is double-buffered and was issued before that PV.
+                    if (i > 0 && nm == 1) {
                         ok = __all_sync(0xffffffffu, mbar_wait(bar(Bars::kO + wg), (jt - 1) & 1, s_abort));
                         tc_fence_after();
                     }
