@@ -2,8 +2,8 @@
 
 Tolerances: max |gpu - oracle| <= 2e-2 for bf16 inputs/outputs, <= 1e-4 for fp32
 (the stated bounds of the verification step).  Small cases are compared on every
-row; the full-size workloads on sampled rows, in the launch configuration the
-benchmark times."""
+row; the full-size workloads, in the launch configuration the benchmark times, on
+rows stratified over the work layout (every unit, row group and M tile)."""
 import numpy as np
 import pytest
 
@@ -75,15 +75,33 @@ def test_many_units_two_row_groups_flagged_in_the_middle():
     _check_all_rows(inp)
 
 
+def _unit_rows(inp, rng):
+    """Rows to compare at full size, stratified over the work layout: in every (sequence,
+    kv head) unit, the first and last row of every 128-row M tile and one random row of
+    each, so every unit, row group and M tile boundary -- and with them every stream-K
+    split and merge -- is checked.  Flat row id = (b*N + n)*Hq + h, unit row r = n*G + j."""
+    B, N, Hq, Hkv = inp["B"], inp["N"], inp["Hq"], inp["Hkv"]
+    G = Hq // Hkv
+    R = N * G
+    picks = []
+    for t0 in range(0, R, 128):
+        t1 = min(R, t0 + 128) - 1
+        picks.append(np.array([t0, t1]))
+        picks.append(rng.integers(t0, t1 + 1, 1))
+    unit_rows = np.unique(np.concatenate(picks))
+    b, g, r = np.meshgrid(np.arange(B), np.arange(Hkv), unit_rows, indexing="ij")
+    n, j = r // G, r % G
+    return np.unique(((b * N + n) * Hq + g * G + j).ravel())
+
+
 @pytest.mark.parametrize("cfg", [1, 2, 3, 4])
 def test_full_size_sampled_rows(cfg):
     inp = W.generate(W.CONFIGS[cfg])
     got, gerr = run_attn(inp)
     assert not gerr.any()
     assert np.isfinite(got).all()
-    rng = np.random.default_rng(cfg)
-    rows = np.unique(np.concatenate([rng.integers(0, got.shape[0], 40), [0, got.shape[0] - 1]]))
+    rows = _unit_rows(inp, np.random.default_rng(cfg))
+    assert len(rows) >= inp["B"] * inp["Hkv"] * 3
     want, _ = oracle.tree_verify_attn(inp, rows)
     err = np.abs(got[rows] - want).max()
     assert err <= TOL[inp["dtype"]], err
-
