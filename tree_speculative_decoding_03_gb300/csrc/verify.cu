@@ -258,14 +258,17 @@ struct __align__(16) RedSlot {
 };
 
 enum { kRedStats = 0, kRedSums = 1, kRedArgmax = 2 };
+constexpr int kMaxCluster = 16;  // CTAs of a walk's cluster
 
-// Cluster all-reduce: every CTA publishes `mine` in its own slot[parity], the
-// cluster synchronises, and warp 0 of every CTA combines all slots in rank order
-// (so every CTA obtains bit-identical results).  Stats: (raw max a, sum hi+lo of
+// Cluster all-reduce: every CTA writes `mine` into slot [parity][its rank] of every CTA
+// of the cluster (remote stores, issued before the barrier), the cluster synchronises,
+// and warp 0 of every CTA combines its own, now local, slots in rank order (so every
+// CTA obtains bit-identical results).  Stats: (raw max a, sum hi+lo of
 // 2^(x c - fl(a c))) with per-slot rescaling; sums: two float-float sums; argmax:
 // (a, i).  Must be called by every thread of every CTA; the result is in *res
-// after the closing __syncthreads.  Slots alternate by parity, so the write of the
-// next reduction cannot overtake a slow CTA still reading this one.
+// after the closing __syncthreads.  Slots alternate by parity, so the writes of the
+// next reduction cannot overtake a slow CTA still reading this one: they follow the
+// next barrier, which the slow CTA passes only after its reads.  slots: [2][kMaxCluster].
 struct NoPost {
     __device__ void operator()(const RedSlot&) const {}
 };
@@ -275,7 +278,7 @@ __device__ __forceinline__ void cluster_allreduce(cg::cluster_group& cluster, Re
                                                   bool wait_async = false, const Post& post = Post()) {
     const int tid = threadIdx.x, lane = tid & 31;
     const int cs = (int)cluster.num_blocks();
-    if (tid == 0) slots[parity] = mine;
+    if (tid < cs) *cluster.map_shared_rank(&slots[parity * kMaxCluster + cluster.block_rank()], tid) = mine;
     // the last warp's asynchronous copies (issued before the row pass) have landed by the
     // cluster barrier, which makes them visible to warp 0's post-step
     if (wait_async && (tid >> 5) == (int)(blockDim.x >> 5) - 1) asm volatile("cp.async.wait_all;" ::: "memory");
@@ -284,7 +287,7 @@ __device__ __forceinline__ void cluster_allreduce(cg::cluster_group& cluster, Re
         RedSlot r{};
         r.a = -INFINITY;
         r.i = 0x7fffffff;
-        if (lane < cs) r = *cluster.map_shared_rank(&slots[parity], lane);
+        if (lane < cs) r = slots[parity * kMaxCluster + lane];
         const int flag = warp_or(lane < cs ? r.flag : 0);
         RedSlot o{};
         o.flag = flag;
@@ -393,7 +396,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
     // whether its token has already been rejected at this node
     __shared__ ff s_px[kMaxNodes], s_qc[kMaxNodes];
     __shared__ int s_rflag[kMaxNodes];
-    __shared__ RedSlot s_red[2];
+    __shared__ RedSlot s_red[2 * kMaxCluster];  // [parity][source rank]
     __shared__ RedSlot s_cta;  // this CTA's partial
     __shared__ RedSlot s_all;  // cluster result
     __shared__ float s_wf[32], s_wg[32];
@@ -1045,13 +1048,13 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
         RedSlot r{};
         r.hi = s_segcum[nseg - 1].hi;  // CTA total
         r.lo = s_segcum[nseg - 1].lo;
-        s_red[parity] = r;
+        s_red[parity * kMaxCluster] = r;
     }
     cluster.sync();
     if (warp == 0) {
         ff tot = ff_make(0.0f);
         if (lane < cs) {
-            const RedSlot* rs = cluster.map_shared_rank(&s_red[parity], lane);
+            const RedSlot* rs = cluster.map_shared_rank(&s_red[parity * kMaxCluster], lane);
             tot = ff{rs->hi, rs->lo};
         }
         ff incl = tot;
