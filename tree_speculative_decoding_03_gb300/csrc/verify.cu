@@ -278,6 +278,9 @@ __device__ __forceinline__ void cluster_allreduce(cg::cluster_group& cluster, Re
                                                   bool wait_async = false, const Post& post = Post()) {
     const int tid = threadIdx.x, lane = tid & 31;
     const int cs = (int)cluster.num_blocks();
+    // `mine` was written by a lane of warp 0 (the callers need no block barrier before the
+    // call: the cluster barrier below holds every thread)
+    if (tid < 32) __syncwarp();
     if (tid < cs) *cluster.map_shared_rank(&slots[parity * kMaxCluster + cluster.block_rank()], tid) = mine;
     // the last warp's asynchronous copies (issued before the row pass) have landed by the
     // cluster barrier, which makes them visible to warp 0's post-step
@@ -446,7 +449,6 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                 s_cta = r;
             }
         }
-        __syncthreads();
         cluster_allreduce(cluster, s_red, parity, s_cta, kRedSums, c2, &s_all);
         parity ^= 1;
     };
@@ -571,7 +573,6 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                     s_cta = m;
                 }
             }
-            __syncthreads();
             cluster_allreduce(cluster, s_red, parity, s_cta, kRedArgmax, c2, &s_all, true);
             parity ^= 1;
             amax = s_all.i;
@@ -617,7 +618,6 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                     s_cta = r;
                 }
             }
-            __syncthreads();
             // warp 0, before the reduction's closing barrier: the children's p(x), q(x) at
             // level 0, one lane per child (p(x) in float-float from a compensated exponent
             // argument; the normaliser is Zf without the rounding of M c2).  The last warp's
@@ -859,7 +859,6 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                     s_cta = r;
                 }
             }
-            __syncthreads();
             cluster_allreduce(cluster, s_red, parity, s_cta, kRedSums, c2, &s_all);
             parity ^= 1;
             if (s_all.flag) {
@@ -1004,7 +1003,6 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                 s_cta = m;
             }
         }
-        __syncthreads();
         cluster_allreduce(cluster, s_red, parity, s_cta, kRedArgmax, c2, &s_all);
         parity ^= 1;
         if (rank == 0 && tid == 0) {
