@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
     const float c2 = greedy ? 0.0f : 1.4426950408889634f / a.T;  // log2(e) / T
 
     __shared__ int s_par[kMaxNodes], s_tok[kMaxNodes], s_path[kMaxNodes];
-    __shared__ int s_kids[kMaxNodes];
+    __shared__ int s_rank[kMaxNodes];  // a child's place among its siblings (set-up only)
     __shared__ float s_lx[kMaxNodes], s_qx[kMaxNodes], s_ux[kMaxNodes];
     // per child of the current node: p(x), q(x) at the current residual level, and
     // whether its token has already been rejected at this node
@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
     __shared__ RedSlot s_all;  // cluster result
     __shared__ float s_wf[32], s_wg[32];
     __shared__ int s_wi[32], s_wb[32];
-    __shared__ int s_nk, s_flag;
+    __shared__ int s_flag;
     // rejection history at the current node
     __shared__ int s_xrej[kMaxRejections];        // rejected tokens x_1..x_j
     __shared__ ff s_zr[kMaxRejections + 1];       // residual sums Zr_j (level j >= 1)
@@ -472,6 +472,45 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
     int err = tree_ok ? 0 : TSV_DERR_PARENT;
     int node = 0, plen = 1;
     if (tid == 0) s_path[0] = 0;
+    // children of every node in index order, once (warp 0): node i's children are
+    // s_kidlist[s_kstart[i] .. s_kstart[i] + s_kcnt[i]).  A child's place among its
+    // siblings is its parent's count so far plus its rank among the lanes of its chunk
+    // with the same parent.
+    __shared__ int s_kcnt[kMaxNodes], s_kstart[kMaxNodes], s_kidlist[kMaxNodes];
+    if (tree_ok && warp == 0) {
+        for (int i = lane; i < N; i += 32) s_kcnt[i] = 0;
+        __syncwarp();
+        for (int base = 1; base < N; base += 32) {
+            const int c = base + lane;
+            const bool has = c < N;
+            const int p = has ? s_par[c] : -1 - lane;  // lanes past N: a parent of their own
+            const unsigned same = __match_any_sync(0xffffffffu, p);
+            const int within = __popc(same & ((1u << lane) - 1u));
+            const int before = has ? s_kcnt[p] : 0;
+            __syncwarp();
+            if (has) {
+                s_rank[c] = before + within;
+                if (within == 0) s_kcnt[p] = before + __popc(same);
+            }
+            __syncwarp();
+        }
+        int carry = 0;  // exclusive prefix of the counts
+        for (int base = 0; base < N; base += 32) {
+            const int i = base + lane;
+            const int v = i < N ? s_kcnt[i] : 0;
+            int incl = v;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                if (lane >= o) incl += y;
+            }
+            if (i < N) s_kstart[i] = carry + incl - v;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        __syncwarp();
+        for (int c = 1 + lane; c < N; c += 32) s_kidlist[s_kstart[s_par[c]] + s_rank[c]] = c;
+    }
+    __syncthreads();
     // the current node's logits slice stays in registers; its draft row is re-read (from
     // L2, where it was prefetched) by the passes that need it, which keeps register
     // pressure low enough for 32 entries per thread
@@ -493,25 +532,14 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
         }
         const TL* lrow = static_cast<const TL*>(a.logits) + ((long long)b * N + node) * V;
         const float* qrow = greedy ? nullptr : a.probs + ((long long)b * N + node) * V;
-        // children of `node`, in index order (warp 0, by ballot)
-        if (warp == 0) {
-            int nk = 0;
-            for (int base = node + 1; base < N; base += 32) {
-                const int c = base + lane;
-                const bool is_kid = c < N && s_par[c] == node;
-                const unsigned m = __ballot_sync(0xffffffffu, is_kid);
-                if (is_kid) s_kids[nk + __popc(m & ((1u << lane) - 1u))] = c;
-                nk += __popc(m);
-            }
-            if (lane == 0) s_nk = nk;
-        }
-        __syncthreads();
-        const int nk = s_nk;
+        // children of `node`, in index order
+        const int nk = s_kcnt[node];
+        const int* kids = s_kidlist + s_kstart[node];
         // the last warp starts asynchronous copies of the scalars the children's tests
         // need (they land while the row is reduced); the rest of the block starts on the row
         if (warp == nwarps - 1) {
             for (int t = lane; t < nk; t += 32) {
-                const int x = s_tok[s_kids[t]];
+                const int x = s_tok[kids[t]];
                 s_qx[t] = 0.0f;
                 if (x >= 0 && x < V) {
                     if (sizeof(TL) == 4)
@@ -520,7 +548,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                         s_lx[t] = to_f32(lrow[x]);  // 2-byte entries: a plain load
                     if (!greedy) {
                         cp_async4(&s_qx[t], qrow + x);
-                        cp_async4(&s_ux[t], a.u_accept + (long long)b * N + s_kids[t]);
+                        cp_async4(&s_ux[t], a.u_accept + (long long)b * N + kids[t]);
                     }
                 }
             }
@@ -528,7 +556,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
         }
         load_slice<VEC, ALIGNED>(lrow, v0, v1, lv, -INFINITY);
         // the first child's logits row into L2, for the likely case that it is accepted
-        if (nk > 0) prefetch_slice<VEC>(static_cast<const TL*>(a.logits) + ((long long)b * N + s_kids[0]) * V, v0, v1);
+        if (nk > 0) prefetch_slice<VEC>(static_cast<const TL*>(a.logits) + ((long long)b * N + kids[0]) * V, v0, v1);
 
         int bad = 0;
 #pragma unroll
@@ -743,7 +771,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
             if (warp == 0) {  // the children's p(x) under the filtered target
                 const ff invZ = ff_recip(ff_mul_f(zkeep, exp2f(-fmaf(M, c2, -MC))));
                 for (int t = lane; t < nk; t += 32) {
-                    const int x = s_tok[s_kids[t]];
+                    const int x = s_tok[kids[t]];
                     const float lx = s_lx[t];
                     const uint32_t key = order_key(lx);
                     const bool kept = key > theta || (key == theta && x < idx_end);
@@ -765,7 +793,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
         bool q_loaded = false;
         int next = -1;
         for (int t = 0; t < nk; ++t) {
-            const int c = s_kids[t];
+            const int c = kids[t];
             const int x = s_tok[c];
             if (x < 0 || x >= V) {
                 err = TSV_DERR_TOKEN;
@@ -893,7 +921,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                     const ff q2 = s_qc[t2];
                     if (zr_ok) p2 = ff_mul(ff_max0(ff_sub(p2, q2)), inv_zr);
                     int rf = s_rflag[t2];
-                    if (s_tok[s_kids[t2]] == x) rf = 1;
+                    if (s_tok[kids[t2]] == x) rf = 1;
                     s_px[t2] = p2;
                     if (!a.replacement)  // with replacement the later children keep the raw q(x)
                         s_qc[t2] = (rf || !ff_pos(sq)) ? ff_make(0.0f) : ff_mul_f(inv_sq, s_qx[t2]);
