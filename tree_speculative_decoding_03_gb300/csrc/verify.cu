@@ -223,15 +223,15 @@ __device__ __forceinline__ void load4(const float* row, int base, int v1, float 
 // xr[0..n-1] (the rejected siblings at the current node): an O(n) scan per pass
 // instead of an O(n) membership test per entry.
 template <int VEC>
-__device__ __forceinline__ uint32_t owned_mask(const int* xr, int n, int v0, int v1) {
-    uint32_t m = 0u;
+__device__ __forceinline__ uint64_t owned_mask(const int* xr, int n, int v0, int v1) {
+    uint64_t m = 0ull;
     for (int i = 0; i < n; ++i) {
         const int x = xr[i];
         if (x < v0 || x >= v1) continue;
         const int f = (x - v0) >> 2;
         if (f % (int)blockDim.x != (int)threadIdx.x) continue;
         const int k = f / (int)blockDim.x;
-        if (k < VEC) m |= 1u << (k * 4 + ((x - v0) & 3));
+        if (k < VEC) m |= 1ull << (k * 4 + ((x - v0) & 3));
     }
     return m;
 }
@@ -378,7 +378,8 @@ __device__ __forceinline__ void fused_compact(const SampleArgs& a, int b, int A,
 }
 
 template <int VEC, bool ALIGNED, typename TL>
-__global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a) {
+// 16 vector steps per thread run with at most 384 threads (168 registers a thread)
+__global__ void __launch_bounds__(VEC > 8 ? 384 : 512, 1) tree_reject_kernel(const SampleArgs a) {
     pdl_wait();  // the inputs may come from the previous kernel in the stream
     pdl_launch_dependents();
     cg::cluster_group cluster = cg::this_cluster();
@@ -411,8 +412,8 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
     __shared__ ff s_sq[kMaxRejections + 1];       // S_j = sum of q over tokens not in {x_1..x_j}
     __shared__ float s_inv_zr[kMaxRejections + 1], s_inv_sq[kMaxRejections + 1];
     __shared__ int s_zr_ok[kMaxRejections + 1];
-    __shared__ float s_seg[8 * 16];  // bonus: [k][warp] segment sums
-    __shared__ ff s_segcum[8 * 16];  // bonus: inclusive prefix over (k, warp)
+    __shared__ float s_seg[16 * 16];  // bonus: [k][warp] segment sums (VEC <= 16, <= 16 warps)
+    __shared__ ff s_segcum[16 * 16];  // bonus: inclusive prefix over (k, warp)
     __shared__ ff s_target;
     __shared__ int s_claim, s_segsel;
     // aligned rows: the first rejection pass at a node keeps this CTA's slice of the
@@ -822,7 +823,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
             // q at this level: the raw row at the node's first pass, and throughout when
             // siblings were drafted independently (with replacement q is never updated)
             const bool raw_q = nrej == 0 || a.replacement;
-            const uint32_t excl = raw_q ? 0u : owned_mask<VEC>(s_xrej, nrej, v0, v1);  // tokens out of q here
+            const uint64_t excl = raw_q ? 0ull : owned_mask<VEC>(s_xrej, nrej, v0, v1);  // tokens out of q here
             const float inv_sq = raw_q ? 1.0f : s_inv_sq[nrej];
             float zr = 0.0f, qs = 0.0f;
             constexpr int QG = VEC < 4 ? VEC : 4;  // draft entries loaded per group of vector steps
@@ -856,7 +857,7 @@ __global__ void __launch_bounds__(512, 1) tree_reject_kernel(const SampleArgs a)
                         if (v < v1 && !isfinite(q)) qb = 1;
                         // p and q at the current level
                         const float p = lv_is_p ? lv[k][e] * pscale : ex2(fmaf(lv[k][e], c2, -MC)) * invZf;
-                        const float qc = raw_q ? q : (((excl >> (k * 4 + e)) & 1u) ? 0.0f : q * inv_sq);
+                        const float qc = raw_q ? q : (((excl >> (k * 4 + e)) & 1ull) ? 0.0f : q * inv_sq);
                         const float d = fmaxf(0.0f, p - qc);
                         zr += d;
                         qs += q;
@@ -1230,12 +1231,12 @@ static int resident_clusters(int cs, int threads, int vpc) {
     return n;
 }
 
-static int vec_for(int V, int cs, int threads, int* vpc_out) {
+static int vec_for(int V, int cs, int threads, int* vpc_out, bool allow16 = false) {
     int vpc = (V + cs - 1) / cs;
     vpc = (vpc + 3) & ~3;
     *vpc_out = vpc;
     const int need = (vpc + threads * 4 - 1) / (threads * 4);
-    return need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : need <= 8 ? 8 : 0;
+    return need <= 1 ? 1 : need <= 2 ? 2 : need <= 4 ? 4 : need <= 8 ? 8 : (allow16 && need <= 16) ? 16 : 0;
 }
 
 template <bool ALIGNED, typename TL>
@@ -1244,6 +1245,7 @@ static int resident_for(int vec, int cs, int threads, int vpc) {
         case 1: return resident_clusters<1, ALIGNED, TL>(cs, threads, vpc);
         case 2: return resident_clusters<2, ALIGNED, TL>(cs, threads, vpc);
         case 4: return resident_clusters<4, ALIGNED, TL>(cs, threads, vpc);
+        case 16: return resident_clusters<16, ALIGNED, TL>(cs, threads, vpc);
         default: return resident_clusters<8, ALIGNED, TL>(cs, threads, vpc);
     }
 }
@@ -1255,6 +1257,7 @@ static cudaError_t launch_vec(const SampleArgs& a, int vec, int B, int cs, int t
         case 2: return launch_reject_inst<2, ALIGNED, TL>(a, B, cs, threads, stream);
         case 4: return launch_reject_inst<4, ALIGNED, TL>(a, B, cs, threads, stream);
         case 8: return launch_reject_inst<8, ALIGNED, TL>(a, B, cs, threads, stream);
+        case 16: return launch_reject_inst<16, ALIGNED, TL>(a, B, cs, threads, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -1289,7 +1292,29 @@ static cudaError_t launch_tree_reject_t(SampleArgs a, int B, int num_sms, cudaSt
         if (res >= B && B * cs <= num_sms) break;
     }
     int vpc;
-    const int vec = vec_for(V, cs, threads, &vpc);
+    int vec = vec_for(V, cs, threads, &vpc);
+    // When the B clusters do not fit at once, 384-thread CTAs with 16 vector steps a thread
+    // (168 registers) hold 1.5x the entries per SM, so more sequences walk at the same time;
+    // a node then costs a little more (a larger slice per CTA), but most of its cost is
+    // latency, so this pays once the resident clusters grow by a fifth.
+    if (threads == 512 && vec == 8) {
+        const int res8 =
+            aligned ? resident_for<true, TL>(vec, cs, threads, vpc) : resident_for<false, TL>(vec, cs, threads, vpc);
+        int cs16 = 1;
+        while (cs16 < 16 && cs16 * 384 * 4 * 16 < V) ++cs16;
+        int vpc16;
+        const int vec16 = vec_for(V, cs16, 384, &vpc16, true);
+        if (res8 < B && vec16 == 16) {
+            const int res16 = aligned ? resident_for<true, TL>(vec16, cs16, 384, vpc16)
+                                      : resident_for<false, TL>(vec16, cs16, 384, vpc16);
+            if (5 * res16 >= 6 * res8) {
+                threads = 384;
+                cs = cs16;
+                vec = vec16;
+                vpc = vpc16;
+            }
+        }
+    }
     a.v_per_cta = vpc;
     return aligned ? launch_vec<true, TL>(a, vec, B, cs, threads, stream)
                    : launch_vec<false, TL>(a, vec, B, cs, threads, stream);
