@@ -116,3 +116,22 @@ def test_filtered_output_follows_the_filtered_target_on_gpu(top_k, top_p):
     m = want > 0
     assert m.sum() >= 2  # a support of one token would make the test trivial
     assert stats.chisquare(counts[m], want[m] * counts.sum()).pvalue > 1e-3
+
+
+@pytest.mark.parametrize("opts", [dict(top_k=50, top_p=0.9), dict(top_k=0, top_p=0.8), dict(with_replacement=True)])
+def test_serving_batch_layout(opts):
+    """The serving mix's batch (64 sequences, 64-node trees, V = 128256) does not fit the
+    512-thread layout at once, so the walk runs 384-thread CTAs with 16 vector steps a
+    thread; the filtered and the with-replacement walks are pinned there too (the
+    prefix plays no part in the walk and is left out)."""
+    w = W.CONFIGS[4].replace(prefix=(0, 0), seed=4040 + len(opts))
+    inp = W.generate(w)
+    T = inp["T"]
+    g = run_verify(inp, **opts)
+    o = oracle.tree_reject_sample(inp, replacement=bool(opts.get("with_replacement", False)),
+                                  top_k=opts.get("top_k", 0), top_p=opts.get("top_p", 1.0))
+    exempt, fails = compare_decisions(inp, g, o, T)
+    B = len(o["accept_len"])
+    msg = f"{opts}: {exempt} of {B} exempt near ties; {len(fails)} mismatches: {fails[:5]}"
+    assert not fails, msg
+    assert exempt <= 0.05 * B + 1, msg
