@@ -395,7 +395,8 @@ __global__ void __launch_bounds__(VEC > 8 ? 384 : 512, 1) tree_reject_kernel(con
 
     __shared__ int s_par[kMaxNodes], s_tok[kMaxNodes], s_path[kMaxNodes];
     __shared__ int s_rank[kMaxNodes];  // a child's place among its siblings (set-up only)
-    __shared__ float s_lx[kMaxNodes], s_qx[kMaxNodes], s_ux[kMaxNodes];
+    // [node parity][child]: a node's copies start while slower warps may still test the previous node's
+    __shared__ float s_lx2[2 * kMaxNodes], s_qx2[2 * kMaxNodes], s_ux2[2 * kMaxNodes];
     // per child of the current node: p(x), q(x) at the current residual level, and
     // whether its token has already been rejected at this node
     __shared__ ff s_px[kMaxNodes], s_qc[kMaxNodes];
@@ -533,9 +534,12 @@ __global__ void __launch_bounds__(VEC > 8 ? 384 : 512, 1) tree_reject_kernel(con
         }
         const TL* lrow = static_cast<const TL*>(a.logits) + ((long long)b * N + node) * V;
         const float* qrow = greedy ? nullptr : a.probs + ((long long)b * N + node) * V;
-        // children of `node`, in index order
+        // children of `node`, in index order, and their scalars' buffers for this node
         const int nk = s_kcnt[node];
         const int* kids = s_kidlist + s_kstart[node];
+        float* s_lx = s_lx2 + (plen & 1) * kMaxNodes;
+        float* s_qx = s_qx2 + (plen & 1) * kMaxNodes;
+        float* s_ux = s_ux2 + (plen & 1) * kMaxNodes;
         // the last warp starts asynchronous copies of the scalars the children's tests
         // need (they land while the row is reduced); the rest of the block starts on the row
         if (warp == nwarps - 1) {
@@ -944,10 +948,11 @@ __global__ void __launch_bounds__(VEC > 8 ? 384 : 512, 1) tree_reject_kernel(con
             }
         }
         if (err || next < 0) break;
+        // no block barrier here: the next node's copies go to the other buffers, and everything
+        // else it writes before its first barrier is read by this node only before one
         if (tid == 0) s_path[plen] = next;
         ++plen;
         node = next;
-        __syncthreads();
     }
 
     if (warp == nwarps - 1) asm volatile("cp.async.wait_all;" ::: "memory");  // no copies in flight at exit
